@@ -1,0 +1,218 @@
+"""Pins for the CPU oracle: hand-computed cases, the pages' worked examples,
+invariants of the definition and brute force on tiny inputs.  CPU only."""
+import numpy as np
+import pytest
+
+import datagen
+import oracle
+from conftest import read_golden
+
+
+def _sets(x, eps):
+    row_ptr, cols, _, _ = oracle.rows(x, eps, np.arange(len(x)), band=0.0)
+    return [set(cols[row_ptr[i]:row_ptr[i + 1]].tolist()) for i in range(len(x))]
+
+
+def test_three_four_five_inclusive():
+    x = np.array([[0.0, 0.0], [3.0, 4.0]], dtype=np.float32)
+    assert _sets(x, 5.0) == [{0, 1}, {0, 1}]          # dist == eps is a neighbour
+    below = np.nextafter(np.float32(5.0), np.float32(0.0))
+    assert _sets(x, below) == [{0}, {1}]
+    assert list(oracle.counts(x, 5.0)) == [2, 2]
+
+
+def test_sphere_16d_exact_boundary():
+    x = np.zeros((4, 16), dtype=np.float32)
+    x[1, :4] = 1.0            # |x1 - x0|^2 = 4 = eps^2
+    x[2, 0] = 2.0             # |x2 - x0|^2 = 4; |x2 - x1|^2 = 1 + 3 = 4
+    x[3, :5] = 1.0            # |x3 - x0|^2 = 5; |x3 - x1|^2 = 1; |x3 - x2|^2 = 1 + 4 = 5
+    got = _sets(x, 2.0)
+    assert got == [{0, 1, 2}, {0, 1, 2, 3}, {0, 1, 2}, {1, 3}]
+
+
+def test_fig3_relation():
+    g = read_golden("fig3_relation.txt")
+    eps = float([v for t, v in g if t == "eps"][0][0])
+    d = int([v for t, v in g if t == "d"][0][0])
+    pts = {int(t[1:]): [float(a) for a in v] for t, v in g if t.startswith("p") and t != "pair"}
+    x = np.zeros((len(pts), d), dtype=np.float32)
+    for i, xy in pts.items():
+        x[i, :2] = xy
+    want = [{i} for i in range(len(pts))]
+    for t, v in g:
+        if t == "pair":
+            i, j = int(v[0]), int(v[1])
+            want[i].add(j)
+            want[j].add(i)
+    assert _sets(x, eps) == want
+    assert oracle.brute_force_py(x, eps) == want
+
+
+def test_fig5_compaction():
+    g = dict(read_golden("fig5_mask.txt"))
+    mask = [int(v) for v in g["mask"]]
+    assert oracle.compact_mask(mask).tolist() == [int(v) for v in g["positions"]]
+
+
+@pytest.mark.parametrize("d", [1, 3, 7, 16])
+def test_brute_force_matches_plain_loops(d):
+    rng = np.random.default_rng(100 + d)
+    x = rng.random((150, d)).astype(np.float32)
+    x[10] = x[3]                              # a duplicate pair
+    eps = float(np.sqrt(d) * 0.25)
+    assert _sets(x, eps) == oracle.brute_force_py(x, eps)
+
+
+def test_invariants_symmetry_self_monotone():
+    x = datagen.generate(1, n=1500)
+    eps_small, eps_big = 0.45, 0.55
+    s1 = _sets(x, eps_small)
+    s2 = _sets(x, eps_big)
+    for i, row in enumerate(s1):
+        assert i in row                                     # self included
+        for j in row:
+            assert i in s1[j]                               # symmetry
+        assert row <= s2[i]                                 # monotone in eps
+    c = oracle.counts(x, eps_small)
+    assert c.tolist() == [len(r) for r in s1]
+
+
+def test_duplicates_single_point_and_eps_zero():
+    x = np.array([[1.0, 2.0, 3.0], [1.0, 2.0, 3.0], [1.0, 2.0, 3.5]], dtype=np.float32)
+    assert _sets(x, 0.0) == [{0, 1}, {0, 1}, {2}]
+    assert _sets(x[:1], 0.0) == [{0}]
+
+
+def test_band_flags():
+    x = np.zeros((3, 2), dtype=np.float32)
+    x[1, 0] = 1.0
+    x[2, 0] = np.float32(1.0 + 2e-6)          # s - eps^2 ~ 4e-6 eps^2: inside the band
+    row_ptr, cols, flag, dist2 = oracle.rows(x, 1.0, [0])
+    assert cols.tolist() == [0, 1, 2]
+    assert flag.tolist() == [0, 1, 1]
+    assert dist2[1] == 1.0
+
+
+def test_pick_eps_sample_identity():
+    x = datagen.generate(1, n=3000)
+    q = datagen.sample_queries(len(x), 100, seed=7)
+    k = 10
+    r = oracle.pick_eps(x, k, q)
+    # brute force: pool every (query, other point) squared distance, sort
+    x64 = x.astype(np.float64)
+    pooled = []
+    for i in q:
+        s = ((x64 - x64[i]) ** 2).sum(axis=1)
+        pooled.append(np.delete(s, i))
+    pooled = np.sort(np.concatenate(pooled))
+    assert r["a"] == pooled[len(q) * k - 1]
+    assert r["b"] == pooled[len(q) * k]
+    e2 = oracle.eps_squared(r["eps"])
+    assert int(np.sum(pooled <= e2)) == len(q) * k            # mean K, self excluded
+
+
+def test_pick_eps_retry_path():
+    # many equal distances force the kept-prefix check to ask for a larger M
+    x = np.zeros((400, 2), dtype=np.float32)
+    x[:, 0] = np.repeat(np.arange(20), 20).astype(np.float32)
+    q = np.arange(0, 400, 40)
+    r = oracle.pick_eps(x, 30, q)
+    assert r["a"] <= r["b"]
+
+
+# ---------------- index pins -----------------------------------------------
+
+def test_morton_known_values_and_roundtrip():
+    assert int(oracle.morton3(1, 0, 0)) == 1
+    assert int(oracle.morton3(0, 1, 0)) == 2
+    assert int(oracle.morton3(0, 0, 1)) == 4
+    assert int(oracle.morton3(3, 3, 3)) == 63
+    assert int(oracle.morton3(2, 0, 0)) == 8
+    top = (1 << 21) - 1
+    assert int(oracle.morton3(top, top, top)) == (1 << 63) - 1
+    rng = np.random.default_rng(3)
+    f = rng.integers(0, 1 << 21, size=(3, 500)).astype(np.uint64)
+    back = oracle.demorton3(oracle.morton3(*f))
+    for k in range(3):
+        assert np.array_equal(back[k], f[k])
+
+
+def test_dim_stats_closed_form_and_ties():
+    x = np.zeros((4, 4), dtype=np.float32)
+    x[:, 0] = [0, 2, 0, 2]        # variance 1
+    x[:, 1] = [1, 1, 1, 1]        # variance 0
+    x[:, 2] = [0, 4, 0, 4]        # variance 4
+    x[:, 3] = [5, 3, 5, 3]        # variance 1 (ties with dim 0)
+    mn, mx, var = oracle.dim_stats(x)
+    assert var.tolist() == [1.0, 0.0, 4.0, 1.0]
+    assert mn.tolist() == [0, 1, 0, 3] and mx.tolist() == [2, 1, 4, 5]
+    assert oracle.variance_order(var).tolist() == [2, 0, 3, 1]
+
+
+def test_grid_hand_case():
+    # index dims: variance order puts dim 1 first, then 0, then 2
+    x = np.array([[0.0, 0.0, 0.0, 9.0],
+                  [0.5, 1.5, 0.0, 9.0],
+                  [0.5, 3.5, 0.0, 9.0],
+                  [0.5, 3.6, 0.0, 9.0],
+                  [0.0, 9.0, 0.1, 9.0]], dtype=np.float32)
+    g = oracle.grid(x, 1.0)
+    assert g["perm"][:3].tolist() == [1, 0, 2]
+    w = 1.0 * (1 + 2 ** -10)
+    assert g["w"] == w
+    cells = (g["fine"] >> np.uint64(g["sub_bits"])).astype(int)
+    assert cells[:, 0].tolist() == [0, 1, 3, 3, 8]          # floor(x_1 / w)
+    assert cells[:, 1].tolist() == [0, 0, 0, 0, 0]
+    b = oracle.count_bound(x, 1.0, g)
+    # cells on dim 1: {0: p0}, {1: p1}, {3: p2, p3}, {8: p4}
+    assert b.tolist() == [2, 2, 2, 2, 1]
+
+
+def test_stencil_matches_brute_force_adjacency():
+    x = datagen.generate(5, n=4000)
+    g = oracle.grid(x, 0.6)
+    st = oracle.stencil(g)
+    cx, cy, cz = [c.astype(int) for c in oracle.demorton3(g["cell_key"])]
+    C = g["cell_key"].size
+    for i in range(0, C, max(1, C // 60)):
+        want = [j for j in range(C)
+                if max(abs(cx[i] - cx[j]), abs(cy[i] - cy[j]), abs(cz[i] - cz[j])) <= 1]
+        assert sorted(st[i]) == want
+        # order: dz outermost, then dy, then dx
+        keys = [(cz[j] - cz[i], cy[j] - cy[i], cx[j] - cx[i]) for j in st[i]]
+        assert keys == sorted(keys)
+
+
+@pytest.mark.parametrize("cfg,n,eps", [(1, 2000, 0.45), (2, 3000, 6.0), (5, 3000, 0.9)])
+def test_count_bound_covers_true_count(cfg, n, eps):
+    x = datagen.generate(cfg, n=n)
+    b = oracle.count_bound(x, eps)
+    c = oracle.counts(x, eps)
+    assert np.all(b >= c)
+    assert np.all(c >= 1)
+
+
+def test_grid_order_is_stable_sort_by_key():
+    x = datagen.generate(2, n=1000)
+    g = oracle.grid(x, 5.0)
+    key = g["key"].tolist()
+    want = sorted(range(len(key)), key=lambda i: (key[i], i))
+    assert g["order"].tolist() == want
+    # points of one cell are contiguous in D' order
+    ck = (g["key"][g["order"]] >> np.uint64(3 * g["sub_bits"])).tolist()
+    seen, last = set(), None
+    for v in ck:
+        if v != last:
+            assert v not in seen
+            seen.add(v)
+            last = v
+
+
+def test_grid_neighbours_within_one_cell():
+    x = datagen.generate(1, n=800)
+    eps = 0.5
+    g = oracle.grid(x, eps)
+    cells = (g["fine"] >> np.uint64(g["sub_bits"])).astype(np.int64)
+    for i, row in enumerate(_sets(x, eps)):
+        for j in row:
+            assert np.max(np.abs(cells[i] - cells[j])) <= 1

@@ -1,0 +1,100 @@
+"""Plant plausible mistakes in copies of the oracle's C source and check that
+the pins catch every one.  The mutants are compiled on the CPU into temporary
+libraries; the real oracle is untouched."""
+import ctypes
+import os
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+import datagen
+import oracle
+from conftest import read_golden
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+MUTANTS = {
+    "dropped_last_term": ("for (int k = 0; k < d; ++k)", "for (int k = 0; k < d - 1; ++k)"),
+    "dropped_first_term": ("for (int k = 0; k < d; ++k)", "for (int k = 1; k < d; ++k)"),
+    "sum_not_difference": ("(double)a[k] - (double)b[k]", "(double)a[k] + (double)b[k]"),
+    "missing_square": ("s += t * t;", "s += t < 0 ? -t : t;"),
+    "row_stride": ("x + j * (int64_t)d, d) <= hi", "x + j, d) <= hi"),
+    "strict_rows": ("if (sqdist(q, x + j * (int64_t)d, d) <= hi)", "if (sqdist(q, x + j * (int64_t)d, d) < hi)"),
+    "strict_counts": ("d, d) <= eps2)", "d, d) < eps2)"),
+    "self_excluded": ("for (int64_t j = 0; j < n; ++j)\n            if (sqdist(q, x + j * (int64_t)d, d) <= hi)",
+                      "for (int64_t j = 0; j < n; ++j)\n            if (j != rows[r] && sqdist(q, x + j * (int64_t)d, d) <= hi)"),
+    "picker_keeps_self": ("if (j != i) buf[m++]", "buf[m++]"),
+    "picker_off_by_one": ("const double a = pool[nq * K - 1], b = pool[nq * K];",
+                          "const double a = pool[nq * K], b = pool[nq * K + 1];"),
+}
+
+
+def _load(path):
+    lib = ctypes.CDLL(path)
+    i64, i32, f64, p = ctypes.c_int64, ctypes.c_int32, ctypes.c_double, ctypes.c_void_p
+    lib.orc_rows_count.argtypes = [p, i64, i32, f64, f64, p, i64, p]
+    lib.orc_counts.argtypes = [p, i64, i32, f64, p]
+    lib.orc_pick_eps2.argtypes = [p, i64, i32, p, i64, i64, i64, p, p]
+    lib.orc_pick_eps2.restype = ctypes.c_int
+    return lib
+
+
+def _pin_cases():
+    cases = []
+    x = np.array([[0.0, 0.0], [3.0, 4.0]], dtype=np.float32)
+    cases.append((x, 5.0, [2, 2]))
+    x = np.zeros((4, 16), dtype=np.float32)
+    x[1, :4] = 1.0
+    x[2, 0] = 2.0
+    x[3, :5] = 1.0
+    cases.append((x, 2.0, [3, 4, 3, 2]))
+    g = read_golden("fig3_relation.txt")
+    pts = {int(t[1:]): [float(a) for a in v] for t, v in g if t.startswith("p") and t != "pair"}
+    x = np.zeros((len(pts), 8), dtype=np.float32)
+    for i, xy in pts.items():
+        x[i, :2] = xy
+    cases.append((x, 1.0, [2, 2, 2, 2, 1, 2, 2]))
+    return cases
+
+
+def _pins_hold(lib) -> bool:
+    for x, eps, want in _pin_cases():
+        n, d = x.shape
+        e2 = oracle.eps_squared(eps)
+        q = np.arange(n, dtype=np.int64)
+        c1 = np.empty(n, dtype=np.int64)
+        lib.orc_rows_count(x.ctypes.data, n, d, e2, 0.0, q.ctypes.data, n, c1.ctypes.data)
+        c2 = np.empty(n, dtype=np.int64)
+        lib.orc_counts(x.ctypes.data, n, d, e2, c2.ctypes.data)
+        if c1.tolist() != want or c2.tolist() != want:
+            return False
+    # epsilon picker against a pooled brute-force sort
+    x = datagen.generate(1, n=600)
+    q = datagen.sample_queries(len(x), 20, seed=3)
+    a, b = ctypes.c_double(), ctypes.c_double()
+    rc = lib.orc_pick_eps2(x.ctypes.data, len(x), x.shape[1], q.ctypes.data, q.size, 5, 599,
+                           ctypes.byref(a), ctypes.byref(b))
+    x64 = x.astype(np.float64)
+    pooled = np.sort(np.concatenate([np.delete(((x64 - x64[i]) ** 2).sum(1), i) for i in q]))
+    return rc == 0 and a.value == pooled[q.size * 5 - 1] and b.value == pooled[q.size * 5]
+
+
+def test_real_oracle_passes_mutant_pins(tmp_path):
+    assert _pins_hold(_load(oracle.build()))
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert old in src, name
+    mutated = src.replace(old, new)
+    c = tmp_path / ("m_%s.c" % name)
+    so = tmp_path / ("m_%s.so" % name)
+    c.write_text(mutated)
+    subprocess.check_call(["gcc", "-O1", "-fopenmp", "-ffp-contract=off", "-shared", "-fPIC",
+                           "-o", str(so), str(c)])
+    assert not _pins_hold(_load(str(so))), "pins did not catch mutant %s" % name
