@@ -1,0 +1,317 @@
+"""Benchmark of the exact epsilon self-join on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl hiss|reference]
+
+One step is the whole hot path on one synthetic workload: hiss_build (variance
+order), hiss_count (grid index + count pass) and hiss_join (batched
+refinement + compaction to CSR, results left on the device).  The default
+workload is the 1,000,000-point, 32-dimensional Gaussian mixture with eps set
+for a mean of 64 neighbours per point.  ``value`` is result pairs per second
+(self pairs included) with the points already resident in device memory;
+``e2e`` is the same metric through the host-buffer entry points (points copied
+in, every batch of results copied out to pinned host memory, both inside the
+timed region).  The L2 cache is flushed (a 512 MB write) before every timed
+step, outside the timed region.
+
+``--impl reference`` times the fp64 CPU oracle (plain brute force) on a
+bounded sample of query rows of the same workload and reports the same
+metric.  Under torchrun each rank runs an independent replica of the
+workload (the join does not need a collective); ``value`` sums all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import datagen  # noqa: E402
+
+METRIC = "eps-self-join result pairs/s (and candidate distance evaluations/s) at 1 GB300"
+UNIT = "pairs/s"
+
+
+def load_eps(cfg):
+    with open(os.path.join(ROOT, "tests", "golden", "eps_configs.json")) as f:
+        return json.load(f)[str(cfg)]["eps"]
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0}, "fallback"
+
+
+def fp32_peak_tflops(sm_mhz):
+    """FP32 pipe peak for the refinement's instruction mix: 152 SMs x 128 FP32
+    lanes x clock; one pair-dimension is a subtract (1 flop) and a fused
+    multiply-add (2 flops) in two lane-instructions, so 1.5 flop per
+    lane-instruction."""
+    return 152 * 128 * sm_mhz * 1e6 * 1.5 / 1e12
+
+
+class Clocks:
+    """nvidia-smi samples during the timed region."""
+
+    FIELDS = "clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown," \
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown," \
+             "clocks_event_reasons.sw_power_cap"
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        out = {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        if not self.path or not os.path.exists(self.path):
+            return out
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            p = [v.strip() for v in line.split(",")]
+            if len(p) < 8:
+                continue
+            try:
+                sm.append(float(p[0]))
+                mx.append(float(p[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, p[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.path)
+        if sm:
+            out.update(sm_mhz=statistics.median(sm), sm_max_mhz=max(mx), reasons=sorted(reasons),
+                       samples=len(sm))
+        return out
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, world, rank):
+    """fp64 CPU oracle on a bounded sample of query rows per step."""
+    if rank != 0:
+        return
+    import oracle
+    name, n, d, k = datagen.CONFIGS[args.config]
+    x = datagen.generate(args.config)
+    eps = load_eps(args.config)
+    rows_per_step = args.ref_rows
+    cores = len(os.sched_getaffinity(0))
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores))
+    rng = np.random.default_rng(12345)
+    times, pairs = [], []
+    for step in range(args.warmup + args.steps):
+        q = rng.choice(n, size=rows_per_step, replace=False)
+        t0 = time.perf_counter()
+        row_ptr, _, _, _ = oracle.rows(x, eps, q, band=0.0)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            times.append(dt)
+            pairs.append(int(row_ptr[-1]))
+    t = sum(times)
+    value = sum(pairs) / t
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(args, eps),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "%d random query rows x all %d points per step (fp64 brute force)"
+                                       % (rows_per_step, n)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "candidate_evals_per_s": rows_per_step * n * args.steps / t}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(args, eps):
+    name, n, d, k = datagen.CONFIGS[args.config]
+    return {"workload": "%s N=%d d=%d mean_neighbours=%d" % (name, n, d, k), "n": n, "d": d, "eps": eps,
+            "eps_hex": float(eps).hex(), "batch_bytes": args.batch_bytes, "l2": "flushed between steps",
+            "parallelism": "replica per GPU"}
+
+
+def cpu_baseline(args, x, eps):
+    """The oracle as it stands on a bounded sample (rank 0, N = 1 only)."""
+    import oracle
+    n = x.shape[0]
+    cores = len(os.sched_getaffinity(0))
+    q = np.random.default_rng(777).choice(n, size=args.ref_rows, replace=False)
+    t0 = time.perf_counter()
+    row_ptr, _, _, _ = oracle.rows(x, eps, q, band=0.0)
+    dt = time.perf_counter() - t0
+    return {"value": int(row_ptr[-1]) / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "%d random query rows x all %d points, fp64 brute force, %.1f s" % (args.ref_rows, n, dt),
+            "candidate_evals_per_s": args.ref_rows * n / dt}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--impl", default="hiss", choices=["hiss", "reference"])
+    ap.add_argument("--batch-bytes", type=int, default=32 << 30)
+    ap.add_argument("--ref-rows", type=int, default=2000)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_env()
+
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import exact_dimensional_distance_gb300 as edd
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    x = datagen.generate(args.config)
+    eps = load_eps(args.config)
+    n, d = x.shape
+    stream = torch.cuda.Stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    with torch.cuda.stream(stream):
+        xd = torch.from_numpy(x).cuda()
+        j = edd.Join(stream)
+    torch.cuda.synchronize()
+
+    def step():
+        j.build(xd)
+        j.count(eps, out=False)
+        return j.join(eps, args.batch_bytes)
+
+    for _ in range(args.warmup):
+        st = step()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    stats = []
+    launches0 = j.launches()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            torch.cuda.synchronize()
+            ev[i][0].record(stream)
+            stats.append(step())
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    launches = j.launches() - launches0
+    ms = [a.elapsed_time(b) for a, b in ev]
+    t_local = sum(ms) / 1e3
+    t = t_local
+    if dist:
+        tt = torch.tensor([t_local], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t = float(tt.item())
+    pairs = stats[-1]["pairs"]
+    cand = stats[-1]["candidates"]
+    value = world * pairs * args.steps / t
+    clocks = clk.summary()
+
+    # roofline of the refinement kernel: per launch (one per batch), the
+    # algorithmic work is 3 flops per candidate pair and dimension
+    st = stats[-1]
+    refine_ms = statistics.median(s["ms_refine"] for s in stats)
+    refine_launches = st["batches"]
+    flops = 3.0 * cand * d
+    pk, pk_kind = peaks()
+    peak = fp32_peak_tflops(pk.get("sm_max_mhz", 2070.0))
+    achieved = flops / (refine_ms / 1e3) / 1e12
+    roofline = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": None, "kernel": "k_refine", "work": "3 flop x candidate pairs x d (no early exit)",
+                "launches_per_step": refine_launches, "ms_per_launch": refine_ms / refine_launches,
+                "peak_kind": "FP32 lanes x %s sm_max_mhz x 1.5 flop" % pk_kind}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": workload_config(args, eps), "gpu_launches": int(launches),
+            "candidate_evals_per_s": world * cand * args.steps / t,
+            "pairs_per_step": pairs, "candidates_per_step": cand,
+            "pruning": 1.0 - cand / float(n) ** 2,
+            "phase_ms": {k: st[k] for k in ("ms_build", "ms_index", "ms_count", "ms_refine", "ms_compact",
+                                            "ms_deliver")},
+            "batches": st["batches"], "cells": st["cells"], "clocks": clocks, "roofline": roofline}
+
+    if not args.no_e2e:
+        # end to end through the host-buffer entry points
+        hx_t = torch.from_numpy(x).pin_memory()
+        hx = hx_t.numpy()
+        d2h = [0]
+
+        def on_batch(b):
+            d2h[0] += 8 * b.nq + 8 * (b.nq + 1) + 4 * b.nq + 4 * b.nnz
+
+        def e2e_step():
+            j.build(hx)
+            j.count(eps, out=False)
+            j.join(eps, args.batch_bytes, edd.HISS_OUT_CSR, True, on_batch)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        d2h[0] = 0
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        torch.cuda.synchronize()
+        te = time.perf_counter() - t0
+        line["e2e"] = {"value": world * pairs * args.steps / te, "unit": UNIT,
+                       "h2d_bytes_per_step": int(x.nbytes), "d2h_bytes_per_step": int(d2h[0] // args.steps),
+                       "ms_per_step": 1e3 * te / args.steps}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args, x, eps)
+    j.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,826 @@
+// C ABI of libhiss.so: context, buffers, and the orchestration of build,
+// count and join (RT-HiSS Sections IV-A to IV-F rebuilt for one GPU without
+// ray-tracing cores).  All device work runs on the context's stream; the
+// host only sizes launches from a few counts it reads back.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "hiss_internal.cuh"
+
+using namespace hiss;
+
+namespace {
+
+struct DBuf {
+    void *p = nullptr;
+    size_t cap = 0;
+};
+
+template <typename T>
+T *as(DBuf &b) { return static_cast<T *>(b.p); }
+
+}  // namespace
+
+struct hiss_ctx {
+    int device = 0;
+    cudaStream_t stream = nullptr;
+    int sticky = 0;
+    char cuda_err[256] = {0};
+    int64_t alloc_limit = 0;
+    int64_t alloc_held = 0;
+    int64_t launches = 0;
+
+    // dataset (variance-ordered, padded to d4)
+    bool built = false;
+    int64_t n = 0;
+    int d = 0, d4 = 0;
+    std::vector<int32_t> perm;
+    std::vector<double> stats;  // [4][d]: min, max, mean, var (original dimension order)
+    DBuf x_stage, xv, perm_d, stats_partial, stats_out, flags;
+
+    // grid index for one eps
+    bool grid_valid = false;
+    float grid_eps = 0.0f;
+    GridParams gp{};
+    int64_t C = 0, cell_pairs = 0, candidates = 0;
+    DBuf keys, vals, keys_alt, vals_alt, sort_tmp, xs, ids, flag, flag_scan, cell_start, cell_key, cell_of_row;
+    DBuf nbr, nbr_cnt, bound, work_key, cell_idx, work, scan_tmp, sums2;
+    uint64_t *sorted_keys = nullptr;
+    uint32_t *sorted_vals = nullptr;
+
+    // query tiles in processing order
+    bool tiles_valid = false;
+    int64_t T = 0, total_units = 0, total_words = 0;
+    DBuf lpt_keys, lpt_order, ntiles, tile_off, tile_cell, tile_q0, tile_nq, tile_word, tile_unit, tile_qoff;
+    uint32_t *order = nullptr;
+
+    // batches
+    DBuf boundaries, binfo, nb_d, mask, qcount, row_ptr, cols, query_ids, query_rows, cand, mask_row_ptr;
+
+    // host staging for copy_to_host
+    void *h_pinned = nullptr;
+    size_t h_cap = 0;
+
+    // test helpers
+    DBuf t_keys_alt, t_vals_alt, t_sort_tmp, t_scan_tmp;
+
+    hiss_stats st{};
+    cudaEvent_t ev[8] = {};
+};
+
+namespace {
+
+constexpr double kCellMargin = 1.0 / 1024.0;  // cell side = eps (1 + 2^-10)
+constexpr int kMortonBits = 21;
+constexpr int kSubBitsMax = 5;
+constexpr int kExtentBits = 20;
+
+int fail_cuda(hiss_ctx *c, cudaError_t e)
+{
+    snprintf(c->cuda_err, sizeof(c->cuda_err), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+    c->sticky = HISS_E_CUDA;
+    return HISS_E_CUDA;
+}
+
+#define CK(expr)                                          \
+    do {                                                  \
+        cudaError_t e__ = (expr);                         \
+        if (e__ != cudaSuccess) return fail_cuda(ctx, e__); \
+    } while (0)
+
+#define ST(expr)                       \
+    do {                               \
+        int r__ = (expr);              \
+        if (r__ != HISS_OK) return r__; \
+    } while (0)
+
+int enter(hiss_ctx *ctx)
+{
+    if (!ctx) return HISS_E_ARG;
+    if (ctx->sticky) return HISS_E_STATE;
+    cudaGetLastError();  // drop a stale non-sticky error left by an earlier runtime call
+    cudaError_t e = cudaSetDevice(ctx->device);
+    if (e != cudaSuccess) return fail_cuda(ctx, e);
+    return HISS_OK;
+}
+
+// Grow-only device buffer on the context's stream.
+int ensure(hiss_ctx *ctx, DBuf &b, size_t bytes)
+{
+    if (bytes == 0) bytes = 16;
+    bytes = (bytes + 255) & ~(size_t)255;
+    if (b.cap >= bytes) return HISS_OK;
+    if (ctx->alloc_limit > 0 && ctx->alloc_held - (int64_t)b.cap + (int64_t)bytes > ctx->alloc_limit)
+        return HISS_E_NOMEM;
+    if (b.p) {
+        CK(cudaFreeAsync(b.p, ctx->stream));
+        ctx->alloc_held -= (int64_t)b.cap;
+        b.p = nullptr;
+        b.cap = 0;
+    }
+    cudaError_t e = cudaMallocAsync(&b.p, bytes, ctx->stream);
+    if (e == cudaErrorMemoryAllocation) {
+        cudaGetLastError();
+        b.p = nullptr;
+        return HISS_E_NOMEM;
+    }
+    CK(e);
+    b.cap = bytes;
+    ctx->alloc_held += (int64_t)bytes;
+    return HISS_OK;
+}
+
+void release(hiss_ctx *ctx, DBuf &b)
+{
+    if (b.p) cudaFreeAsync(b.p, ctx->stream);
+    b.p = nullptr;
+    b.cap = 0;
+}
+
+int sync(hiss_ctx *ctx)
+{
+    CK(cudaStreamSynchronize(ctx->stream));
+    return HISS_OK;
+}
+
+float elapsed(hiss_ctx *ctx, int a, int b)
+{
+    float ms = 0.0f;
+    if (cudaEventElapsedTime(&ms, ctx->ev[a], ctx->ev[b]) != cudaSuccess) {
+        cudaGetLastError();
+        return 0.0f;
+    }
+    return ms;
+}
+
+int check_flags(hiss_ctx *ctx)
+{
+    int h[kNumFlags];
+    CK(cudaMemcpyAsync(h, ctx->flags.p, sizeof(h), cudaMemcpyDeviceToHost, ctx->stream));
+    ST(sync(ctx));
+    if (h[kFlagSortTimeout]) {
+        snprintf(ctx->cuda_err, sizeof(ctx->cuda_err), "radix sort look-back exceeded its wait limit");
+        ctx->sticky = HISS_E_CUDA;
+        return HISS_E_CUDA;
+    }
+    return HISS_OK;
+}
+
+int bit_length(int64_t v)
+{
+    int b = 0;
+    while (v > 0) {
+        ++b;
+        v >>= 1;
+    }
+    return b;
+}
+
+// ---- build -------------------------------------------------------------------
+int do_build(hiss_ctx *ctx, const float *d_points, int64_t n, int32_t d)
+{
+    ctx->built = false;
+    ctx->grid_valid = false;
+    ctx->tiles_valid = false;
+    ctx->st = hiss_stats{};
+    const int64_t launches0 = ctx->launches;
+    CK(cudaEventRecord(ctx->ev[0], ctx->stream));
+    const int d4 = (d + 3) & ~3;
+    const int64_t nb = stats_blocks(n, d);
+    ST(ensure(ctx, ctx->stats_partial, sizeof(double) * (size_t)nb * d * 4));
+    ST(ensure(ctx, ctx->stats_out, sizeof(double) * 4 * (size_t)d + 16));
+    ST(ensure(ctx, ctx->flags, sizeof(int) * kNumFlags * 2));
+    CK(cudaMemsetAsync(ctx->flags.p, 0, sizeof(int) * kNumFlags * 2, ctx->stream));
+    int *nonfinite_d = as<int>(ctx->flags) + kNumFlags;
+    CK(dim_stats(d_points, n, d, as<double>(ctx->stats_partial), as<double>(ctx->stats_out), nonfinite_d,
+                 ctx->stream, &ctx->launches));
+    ctx->stats.assign(4 * (size_t)d, 0.0);
+    int nonfinite = 0;
+    CK(cudaMemcpyAsync(ctx->stats.data(), ctx->stats_out.p, sizeof(double) * 4 * d, cudaMemcpyDeviceToHost,
+                       ctx->stream));
+    CK(cudaMemcpyAsync(&nonfinite, nonfinite_d, sizeof(int), cudaMemcpyDeviceToHost, ctx->stream));
+    ST(sync(ctx));
+    if (nonfinite) return HISS_E_ARG;
+
+    // variance order, descending; equal variances keep the lower index first
+    ctx->perm.resize(d);
+    for (int k = 0; k < d; ++k) ctx->perm[k] = k;
+    const double *var = ctx->stats.data() + 3 * (size_t)d;
+    std::stable_sort(ctx->perm.begin(), ctx->perm.end(), [var](int a, int b) { return var[a] > var[b]; });
+
+    ST(ensure(ctx, ctx->perm_d, sizeof(int32_t) * d));
+    ST(ensure(ctx, ctx->xv, sizeof(float) * (size_t)n * d4));
+    CK(cudaMemcpyAsync(ctx->perm_d.p, ctx->perm.data(), sizeof(int32_t) * d, cudaMemcpyHostToDevice, ctx->stream));
+    CK(permute_pad(d_points, n, d, d4, as<int32_t>(ctx->perm_d), as<float>(ctx->xv), ctx->stream, &ctx->launches));
+    CK(cudaEventRecord(ctx->ev[1], ctx->stream));
+    ST(sync(ctx));
+    ctx->n = n;
+    ctx->d = d;
+    ctx->d4 = d4;
+    ctx->built = true;
+    ctx->st.n = n;
+    ctx->st.d = d;
+    ctx->st.d_pad = d4;
+    ctx->st.ms_build = elapsed(ctx, 0, 1);
+    ctx->st.kernel_launches = ctx->launches - launches0;
+    return HISS_OK;
+}
+
+// ---- grid index for eps --------------------------------------------------------
+int ensure_grid(hiss_ctx *ctx, float eps)
+{
+    if (!ctx->built) return HISS_E_STATE;
+    if (!(eps >= 0.0f) || std::isinf(eps)) return HISS_E_ARG;
+    if (ctx->grid_valid && ctx->grid_eps == eps) return HISS_OK;
+    ctx->grid_valid = false;
+    ctx->tiles_valid = false;
+    const int64_t n = ctx->n;
+    const int d = ctx->d, d4 = ctx->d4;
+    cudaStream_t s = ctx->stream;
+
+    // grid parameters (fp64 on the host, identical to an fp64 reading)
+    GridParams gp{};
+    gp.ndim = d < 3 ? d : 3;
+    double extent = 0.0, ext[3] = {0.0, 0.0, 0.0};
+    for (int k = 0; k < gp.ndim; ++k) {
+        const int dim = ctx->perm[k];
+        const double mn = ctx->stats[0 * (size_t)d + dim], mx = ctx->stats[1 * (size_t)d + dim];
+        gp.origin[k] = mn;
+        ext[k] = mx - mn;
+        extent = std::max(extent, ext[k]);
+    }
+    double w = std::max((double)eps * (1.0 + kCellMargin), std::ldexp(extent, -kExtentBits));
+    if (w == 0.0) w = 1.0;
+    gp.w = w;
+    int64_t cellmax = 0;
+    for (int k = 0; k < gp.ndim; ++k) cellmax = std::max(cellmax, (int64_t)std::floor(ext[k] / w));
+    const int cellbits = bit_length(cellmax);
+    gp.sub_bits = std::min(kSubBitsMax, kMortonBits - cellbits);
+    gp.key_bits = 3 * (cellbits + gp.sub_bits);
+
+    CK(cudaEventRecord(ctx->ev[0], s));
+    ST(ensure(ctx, ctx->keys, 8 * (size_t)n));
+    ST(ensure(ctx, ctx->vals, 4 * (size_t)n));
+    ST(ensure(ctx, ctx->keys_alt, 8 * (size_t)n));
+    ST(ensure(ctx, ctx->vals_alt, 4 * (size_t)n));
+    ST(ensure(ctx, ctx->sort_tmp, sort_tmp_bytes(n)));
+    ST(ensure(ctx, ctx->xs, sizeof(float) * (size_t)n * d4));
+    ST(ensure(ctx, ctx->ids, 4 * (size_t)n));
+    ST(ensure(ctx, ctx->flag, 4 * (size_t)n));
+    ST(ensure(ctx, ctx->flag_scan, 4 * (size_t)(n + 1)));
+    ST(ensure(ctx, ctx->cell_of_row, 4 * (size_t)n));
+    ST(ensure(ctx, ctx->scan_tmp, 8 * (size_t)scan_tmp_elems(n + 1) + 64));
+
+    CK(cell_keys(as<float>(ctx->xv), n, d4, gp, as<uint64_t>(ctx->keys), as<uint32_t>(ctx->vals), s,
+                 &ctx->launches));
+    int in_alt = 0;
+    CK(sort_pairs(as<uint64_t>(ctx->keys), as<uint32_t>(ctx->vals), as<uint64_t>(ctx->keys_alt),
+                  as<uint32_t>(ctx->vals_alt), n, gp.key_bits, ctx->sort_tmp.p, as<int>(ctx->flags), s,
+                  &ctx->launches, &in_alt));
+    ctx->sorted_keys = in_alt ? as<uint64_t>(ctx->keys_alt) : as<uint64_t>(ctx->keys);
+    ctx->sorted_vals = in_alt ? as<uint32_t>(ctx->vals_alt) : as<uint32_t>(ctx->vals);
+    CK(gather_rows(as<float>(ctx->xv), ctx->sorted_vals, n, d4, as<float>(ctx->xs), as<int32_t>(ctx->ids), s,
+                   &ctx->launches));
+    const int shift = 3 * gp.sub_bits;
+    CK(cell_flags(ctx->sorted_keys, n, shift, as<int32_t>(ctx->flag), s, &ctx->launches));
+    CK(scan_i32(as<int32_t>(ctx->flag), as<int32_t>(ctx->flag_scan), n, as<int64_t>(ctx->scan_tmp), s,
+                &ctx->launches));
+    int32_t C32 = 0;
+    CK(cudaMemcpyAsync(&C32, as<int32_t>(ctx->flag_scan) + n, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+    ST(sync(ctx));
+    ST(check_flags(ctx));
+    const int64_t C = C32;
+
+    ST(ensure(ctx, ctx->cell_start, 4 * (size_t)(C + 1)));
+    ST(ensure(ctx, ctx->cell_key, 8 * (size_t)C));
+    ST(ensure(ctx, ctx->nbr, 4 * (size_t)C * kStencil));
+    ST(ensure(ctx, ctx->nbr_cnt, 4 * (size_t)(C + 1)));
+    ST(ensure(ctx, ctx->bound, 8 * (size_t)(C + 1)));
+    ST(ensure(ctx, ctx->work_key, 8 * (size_t)C));
+    ST(ensure(ctx, ctx->cell_idx, 4 * (size_t)C));
+    ST(ensure(ctx, ctx->work, 8 * (size_t)(C + 1)));
+    ST(ensure(ctx, ctx->sums2, 8 * (size_t)(C + 1)));
+    CK(cell_starts(ctx->sorted_keys, as<int32_t>(ctx->flag_scan), n, shift, as<int32_t>(ctx->cell_start),
+                   as<uint64_t>(ctx->cell_key), as<int32_t>(ctx->cell_of_row), s, &ctx->launches));
+    CK(stencil(as<uint64_t>(ctx->cell_key), as<int32_t>(ctx->cell_start), C, as<int32_t>(ctx->nbr),
+               as<int32_t>(ctx->nbr_cnt), as<int64_t>(ctx->bound), as<uint64_t>(ctx->work_key),
+               as<uint32_t>(ctx->cell_idx), as<int64_t>(ctx->work), s, &ctx->launches));
+    // totals: candidates = sum |cell| B_cell, cell pairs = sum of stencil sizes
+    CK(scan_i64(as<int64_t>(ctx->work), as<int64_t>(ctx->sums2), C, as<int64_t>(ctx->scan_tmp), s, &ctx->launches));
+    int64_t tot[2] = {0, 0};
+    CK(cudaMemcpyAsync(&tot[0], as<int64_t>(ctx->sums2) + C, 8, cudaMemcpyDeviceToHost, s));
+    CK(scan_i32_to_i64(as<int32_t>(ctx->nbr_cnt), as<int64_t>(ctx->sums2), C, as<int64_t>(ctx->scan_tmp), s,
+                       &ctx->launches));
+    CK(cudaMemcpyAsync(&tot[1], as<int64_t>(ctx->sums2) + C, 8, cudaMemcpyDeviceToHost, s));
+    CK(cudaEventRecord(ctx->ev[1], s));
+    ST(sync(ctx));
+
+    ctx->gp = gp;
+    ctx->C = C;
+    ctx->candidates = tot[0];
+    ctx->cell_pairs = tot[1];
+    ctx->grid_eps = eps;
+    ctx->grid_valid = true;
+    ctx->st.ms_index = elapsed(ctx, 0, 1);
+    return HISS_OK;
+}
+
+void fill_grid_stats(hiss_ctx *ctx)
+{
+    ctx->st.n = ctx->n;
+    ctx->st.d = ctx->d;
+    ctx->st.d_pad = ctx->d4;
+    ctx->st.cells = ctx->C;
+    ctx->st.cell_pairs = ctx->cell_pairs;
+    ctx->st.candidates = ctx->candidates;
+    ctx->st.sub_bits = ctx->gp.sub_bits;
+    ctx->st.key_bits = ctx->gp.key_bits;
+    ctx->st.cell_width = ctx->gp.w;
+    ctx->st.eps = ctx->grid_eps;
+}
+
+}  // namespace
+
+namespace {
+
+// ---- query tiles in processing order (largest work first) ------------------------
+int ensure_tiles(hiss_ctx *ctx)
+{
+    if (ctx->tiles_valid) return HISS_OK;
+    cudaStream_t s = ctx->stream;
+    const int64_t C = ctx->C;
+    const int tq = refine_tq(ctx->d4), chunk = refine_chunk(ctx->d4);
+    ST(ensure(ctx, ctx->lpt_keys, 8 * (size_t)C));
+    ST(ensure(ctx, ctx->lpt_order, 4 * (size_t)C));
+    ST(ensure(ctx, ctx->ntiles, 4 * (size_t)C));
+    ST(ensure(ctx, ctx->tile_off, 8 * (size_t)(C + 1)));
+    ST(ensure(ctx, ctx->sort_tmp, sort_tmp_bytes(C)));
+    ST(ensure(ctx, ctx->scan_tmp, 8 * (size_t)scan_tmp_elems(C + 1) + 64));
+    // the work keys are consumed by the sort; copy them so the index stays intact
+    CK(cudaMemcpyAsync(ctx->lpt_keys.p, ctx->work_key.p, 8 * (size_t)C, cudaMemcpyDeviceToDevice, s));
+    CK(cudaMemcpyAsync(ctx->lpt_order.p, ctx->cell_idx.p, 4 * (size_t)C, cudaMemcpyDeviceToDevice, s));
+    int in_alt = 0;
+    ST(ensure(ctx, ctx->keys_alt, 8 * (size_t)C));
+    ST(ensure(ctx, ctx->vals_alt, 4 * (size_t)C));
+    CK(sort_pairs(as<uint64_t>(ctx->lpt_keys), as<uint32_t>(ctx->lpt_order), as<uint64_t>(ctx->keys_alt),
+                  as<uint32_t>(ctx->vals_alt), C, 64, ctx->sort_tmp.p, as<int>(ctx->flags), s, &ctx->launches,
+                  &in_alt));
+    if (in_alt)
+        CK(cudaMemcpyAsync(ctx->lpt_order.p, ctx->vals_alt.p, 4 * (size_t)C, cudaMemcpyDeviceToDevice, s));
+    ctx->order = as<uint32_t>(ctx->lpt_order);
+    // keys_alt / vals_alt held the sorted grid keys: the index keeps only the
+    // gathered points, ids and cell arrays, so they are free to reuse here.
+    ctx->sorted_keys = nullptr;
+    ctx->sorted_vals = nullptr;
+
+    CK(tile_counts(ctx->order, as<int32_t>(ctx->cell_start), C, tq, as<int32_t>(ctx->ntiles), s, &ctx->launches));
+    CK(scan_i32_to_i64(as<int32_t>(ctx->ntiles), as<int64_t>(ctx->tile_off), C, as<int64_t>(ctx->scan_tmp), s,
+                       &ctx->launches));
+    int64_t T = 0;
+    CK(cudaMemcpyAsync(&T, as<int64_t>(ctx->tile_off) + C, 8, cudaMemcpyDeviceToHost, s));
+    ST(sync(ctx));
+    ST(check_flags(ctx));
+    ST(ensure(ctx, ctx->tile_cell, 4 * (size_t)T));
+    ST(ensure(ctx, ctx->tile_q0, 4 * (size_t)T));
+    ST(ensure(ctx, ctx->tile_nq, 4 * (size_t)(T + 1)));
+    ST(ensure(ctx, ctx->tile_word, 8 * (size_t)(T + 1)));
+    ST(ensure(ctx, ctx->tile_unit, 8 * (size_t)(T + 1)));
+    ST(ensure(ctx, ctx->tile_qoff, 8 * (size_t)(T + 1)));
+    ST(ensure(ctx, ctx->scan_tmp, 8 * (size_t)scan_tmp_elems(T + 1) + 64));
+    CK(tile_fill(ctx->order, as<int32_t>(ctx->cell_start), as<int64_t>(ctx->bound), as<int64_t>(ctx->tile_off), C,
+                 tq, chunk, as<int32_t>(ctx->tile_cell), as<int32_t>(ctx->tile_q0), as<int32_t>(ctx->tile_nq),
+                 as<int64_t>(ctx->tile_word), as<int64_t>(ctx->tile_unit), s, &ctx->launches));
+    CK(scan_i64(as<int64_t>(ctx->tile_word), as<int64_t>(ctx->tile_word), T, as<int64_t>(ctx->scan_tmp), s,
+                &ctx->launches));
+    CK(scan_i64(as<int64_t>(ctx->tile_unit), as<int64_t>(ctx->tile_unit), T, as<int64_t>(ctx->scan_tmp), s,
+                &ctx->launches));
+    CK(scan_i32_to_i64(as<int32_t>(ctx->tile_nq), as<int64_t>(ctx->tile_qoff), T, as<int64_t>(ctx->scan_tmp), s,
+                       &ctx->launches));
+    int64_t tot[2] = {0, 0};
+    CK(cudaMemcpyAsync(&tot[0], as<int64_t>(ctx->tile_word) + T, 8, cudaMemcpyDeviceToHost, s));
+    CK(cudaMemcpyAsync(&tot[1], as<int64_t>(ctx->tile_unit) + T, 8, cudaMemcpyDeviceToHost, s));
+    ST(sync(ctx));
+    ctx->T = T;
+    ctx->total_words = tot[0];
+    ctx->total_units = tot[1];
+    ctx->tiles_valid = true;
+    return HISS_OK;
+}
+
+int ensure_pinned(hiss_ctx *ctx, size_t bytes)
+{
+    if (ctx->h_cap >= bytes) return HISS_OK;
+    if (ctx->h_pinned) cudaFreeHost(ctx->h_pinned);
+    ctx->h_pinned = nullptr;
+    ctx->h_cap = 0;
+    cudaError_t e = cudaMallocHost(&ctx->h_pinned, bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return HISS_E_NOMEM;
+    }
+    ctx->h_cap = bytes;
+    return HISS_OK;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+int do_join(hiss_ctx *ctx, float eps, size_t batch_bytes, const hiss_out *out)
+{
+    const int mode = out ? out->mode : HISS_OUT_CSR;
+    if (mode != HISS_OUT_CSR && mode != HISS_OUT_MASK) return HISS_E_ARG;
+    const int to_host = out ? out->copy_to_host : 0;
+    hiss_batch_fn fn = out ? out->on_batch : nullptr;
+    void *user = out ? out->user : nullptr;
+    cudaStream_t s = ctx->stream;
+    const int64_t launches0 = ctx->launches;
+    double ms_index = 0.0;
+    if (!(ctx->grid_valid && ctx->grid_eps == eps)) {
+        ST(ensure_grid(ctx, eps));
+        ms_index = ctx->st.ms_index;
+    }
+    CK(cudaEventRecord(ctx->ev[2], s));
+    ST(ensure_tiles(ctx));
+    CK(cudaEventRecord(ctx->ev[3], s));
+
+    if (batch_bytes == 0) {
+        size_t fr = 0, tot = 0;
+        CK(cudaMemGetInfo(&fr, &tot));
+        batch_bytes = fr / 4;
+    }
+    const int64_t cap_words = (int64_t)(batch_bytes / 4);
+    const int64_t T = ctx->T;
+    ST(ensure(ctx, ctx->boundaries, 8 * (size_t)(T + 2)));
+    ST(ensure(ctx, ctx->binfo, 32 * (size_t)(T + 2)));
+    ST(ensure(ctx, ctx->nb_d, 64));
+    CK(cudaMemsetAsync(ctx->flags.p, 0, sizeof(int) * kNumFlags, s));
+    CK(plan_batches(as<int64_t>(ctx->tile_word), as<int64_t>(ctx->tile_unit), as<int64_t>(ctx->tile_qoff), T,
+                    cap_words, as<int64_t>(ctx->boundaries), as<int64_t>(ctx->binfo), as<int64_t>(ctx->nb_d),
+                    as<int>(ctx->flags), s, &ctx->launches));
+    int64_t nb = 0;
+    int hflags[kNumFlags];
+    CK(cudaMemcpyAsync(&nb, ctx->nb_d.p, 8, cudaMemcpyDeviceToHost, s));
+    CK(cudaMemcpyAsync(hflags, ctx->flags.p, sizeof(hflags), cudaMemcpyDeviceToHost, s));
+    ST(sync(ctx));
+    if (hflags[kFlagPlanTooSmall]) return HISS_E_BATCH_TOO_SMALL;
+    std::vector<int64_t> info(4 * (size_t)(nb + 1));
+    CK(cudaMemcpyAsync(info.data(), ctx->binfo.p, 32 * (size_t)(nb + 1), cudaMemcpyDeviceToHost, s));
+    ST(sync(ctx));
+
+    int64_t max_words = 0, max_nq = 0;
+    for (int64_t b = 0; b < nb; ++b) {
+        max_words = std::max(max_words, info[4 * (b + 1)] - info[4 * b]);
+        max_nq = std::max(max_nq, info[4 * (b + 1) + 2] - info[4 * b + 2]);
+    }
+    ST(ensure(ctx, ctx->mask, 4 * (size_t)max_words));
+    ST(ensure(ctx, ctx->qcount, 4 * (size_t)(max_nq + 1)));
+    ST(ensure(ctx, ctx->row_ptr, 8 * (size_t)(max_nq + 1)));
+    ST(ensure(ctx, ctx->query_ids, 8 * (size_t)max_nq));
+    ST(ensure(ctx, ctx->query_rows, 4 * (size_t)max_nq));
+    ST(ensure(ctx, ctx->scan_tmp, 8 * (size_t)scan_tmp_elems(max_nq + 1) + 64));
+    if (mode == HISS_OUT_MASK) {
+        ST(ensure(ctx, ctx->cand, 8 * (size_t)max_nq));
+        ST(ensure(ctx, ctx->mask_row_ptr, 8 * (size_t)(max_nq + 1)));
+    }
+
+    double ms_refine = 0.0, ms_compact = 0.0, ms_deliver = 0.0;
+    int64_t pairs = 0;
+    for (int64_t b = 0; b < nb; ++b) {
+        const int64_t *lo = &info[4 * b], *hi = &info[4 * (b + 1)];
+        const int64_t nq = hi[2] - lo[2];
+        const int64_t nwords = hi[0] - lo[0];
+        CK(cudaMemsetAsync(ctx->qcount.p, 0, 4 * (size_t)nq, s));
+        RefineArgs ra{};
+        ra.xs = as<float>(ctx->xs);
+        ra.cell_start = as<int32_t>(ctx->cell_start);
+        ra.nbr = as<int32_t>(ctx->nbr);
+        ra.nbr_cnt = as<int32_t>(ctx->nbr_cnt);
+        ra.bound = as<int64_t>(ctx->bound);
+        ra.tile_cell = as<int32_t>(ctx->tile_cell);
+        ra.tile_q0 = as<int32_t>(ctx->tile_q0);
+        ra.tile_nq = as<int32_t>(ctx->tile_nq);
+        ra.tile_word = as<int64_t>(ctx->tile_word);
+        ra.tile_unit = as<int64_t>(ctx->tile_unit);
+        ra.tile_qoff = as<int64_t>(ctx->tile_qoff);
+        ra.t0 = lo[3];
+        ra.t1 = hi[3];
+        ra.unit0 = lo[1];
+        ra.nunits = hi[1] - lo[1];
+        ra.word0 = lo[0];
+        ra.q0 = lo[2];
+        ra.mask = as<uint32_t>(ctx->mask);
+        ra.qcount = as<int32_t>(ctx->qcount);
+        ra.d4 = ctx->d4;
+        ra.eps2 = eps * eps;
+        CK(cudaEventRecord(ctx->ev[4], s));
+        CK(refine(ra, s, &ctx->launches));
+        CK(cudaEventRecord(ctx->ev[5], s));
+
+        CompactArgs ca{};
+        ca.ids = as<int32_t>(ctx->ids);
+        ca.cell_start = ra.cell_start;
+        ca.nbr = ra.nbr;
+        ca.nbr_cnt = ra.nbr_cnt;
+        ca.bound = ra.bound;
+        ca.tile_cell = ra.tile_cell;
+        ca.tile_q0 = ra.tile_q0;
+        ca.tile_word = ra.tile_word;
+        ca.tile_qoff = ra.tile_qoff;
+        ca.t0 = ra.t0;
+        ca.t1 = ra.t1;
+        ca.word0 = ra.word0;
+        ca.q0 = ra.q0;
+        ca.nq = nq;
+        ca.mask = ra.mask;
+        ca.query_ids = as<int64_t>(ctx->query_ids);
+        ca.query_rows = as<int32_t>(ctx->query_rows);
+        int64_t nnz = 0;
+        CK(scan_i32_to_i64(as<int32_t>(ctx->qcount), as<int64_t>(ctx->row_ptr), nq, as<int64_t>(ctx->scan_tmp), s,
+                           &ctx->launches));
+        CK(cudaMemcpyAsync(&nnz, as<int64_t>(ctx->row_ptr) + nq, 8, cudaMemcpyDeviceToHost, s));
+        ST(sync(ctx));
+        if (mode == HISS_OUT_CSR) {
+            ST(ensure(ctx, ctx->cols, 4 * (size_t)nnz));
+            ca.row_ptr = as<int64_t>(ctx->row_ptr);
+            ca.cols = as<int32_t>(ctx->cols);
+        } else {
+            ca.cand = as<int64_t>(ctx->cand);
+            ca.mask_row_ptr = as<int64_t>(ctx->mask_row_ptr);
+        }
+        CK(compact(ca, s, &ctx->launches));
+        CK(cudaEventRecord(ctx->ev[6], s));
+
+        hiss_batch hb{};
+        hb.index = b;
+        hb.nq = nq;
+        hb.nnz = nnz;
+        hb.mode = mode;
+        hb.n_words = mode == HISS_OUT_MASK ? nwords : 0;
+        if (to_host) {
+            const size_t o_ids = 0, o_rp = align256(8 * nq), o_rows = o_rp + align256(8 * (nq + 1));
+            const size_t o_cand = o_rows + align256(4 * nq), o_data = o_cand + align256(8 * nq);
+            const size_t bytes = o_data + (mode == HISS_OUT_CSR ? 4 * (size_t)nnz : 4 * (size_t)nwords) + 256;
+            ST(ensure_pinned(ctx, bytes));
+            char *h = static_cast<char *>(ctx->h_pinned);
+            CK(cudaMemcpyAsync(h + o_ids, ctx->query_ids.p, 8 * nq, cudaMemcpyDeviceToHost, s));
+            CK(cudaMemcpyAsync(h + o_rows, ctx->query_rows.p, 4 * nq, cudaMemcpyDeviceToHost, s));
+            if (mode == HISS_OUT_CSR) {
+                CK(cudaMemcpyAsync(h + o_rp, ctx->row_ptr.p, 8 * (nq + 1), cudaMemcpyDeviceToHost, s));
+                CK(cudaMemcpyAsync(h + o_data, ctx->cols.p, 4 * (size_t)nnz, cudaMemcpyDeviceToHost, s));
+                hb.cols = reinterpret_cast<const int32_t *>(h + o_data);
+            } else {
+                CK(cudaMemcpyAsync(h + o_rp, ctx->mask_row_ptr.p, 8 * (nq + 1), cudaMemcpyDeviceToHost, s));
+                CK(cudaMemcpyAsync(h + o_cand, ctx->cand.p, 8 * nq, cudaMemcpyDeviceToHost, s));
+                CK(cudaMemcpyAsync(h + o_data, ctx->mask.p, 4 * (size_t)nwords, cudaMemcpyDeviceToHost, s));
+                hb.mask = reinterpret_cast<const uint32_t *>(h + o_data);
+                hb.cand = reinterpret_cast<const int64_t *>(h + o_cand);
+            }
+            hb.query_ids = reinterpret_cast<const int64_t *>(h + o_ids);
+            hb.row_ptr = reinterpret_cast<const int64_t *>(h + o_rp);
+            hb.query_rows = reinterpret_cast<const int32_t *>(h + o_rows);
+            hb.on_host = 1;
+        } else {
+            hb.query_ids = as<int64_t>(ctx->query_ids);
+            hb.query_rows = as<int32_t>(ctx->query_rows);
+            if (mode == HISS_OUT_CSR) {
+                hb.row_ptr = as<int64_t>(ctx->row_ptr);
+                hb.cols = as<int32_t>(ctx->cols);
+            } else {
+                hb.row_ptr = as<int64_t>(ctx->mask_row_ptr);
+                hb.mask = as<uint32_t>(ctx->mask);
+                hb.cand = as<int64_t>(ctx->cand);
+            }
+        }
+        CK(cudaEventRecord(ctx->ev[7], s));
+        ST(sync(ctx));
+        ms_refine += elapsed(ctx, 4, 5);
+        ms_compact += elapsed(ctx, 5, 6);
+        ms_deliver += elapsed(ctx, 6, 7);
+        pairs += nnz;
+        if (fn && fn(user, &hb) != 0) return HISS_E_CALLBACK;
+    }
+    ST(check_flags(ctx));
+    fill_grid_stats(ctx);
+    ctx->st.pairs = mode == HISS_OUT_CSR ? pairs : -1;
+    ctx->st.batches = nb;
+    ctx->st.query_tiles = T;
+    ctx->st.refine_units = ctx->total_units;
+    ctx->st.mask_words_max = max_words;
+    ctx->st.ms_index = ms_index;
+    ctx->st.ms_count = elapsed(ctx, 2, 3);
+    ctx->st.ms_refine = ms_refine;
+    ctx->st.ms_compact = ms_compact;
+    ctx->st.ms_deliver = ms_deliver;
+    ctx->st.ms_total = ms_index + ctx->st.ms_count + ms_refine + ms_compact + ms_deliver;
+    ctx->st.kernel_launches = ctx->launches - launches0;
+    return HISS_OK;
+}
+
+}  // namespace
+
+// ============================================================================
+// C ABI
+// ============================================================================
+extern "C" {
+
+int hiss_create(hiss_ctx **out, void *cuda_stream)
+{
+    if (!out) return HISS_E_ARG;
+    *out = nullptr;
+    hiss_ctx *ctx = new (std::nothrow) hiss_ctx();
+    if (!ctx) return HISS_E_NOMEM;
+    if (cudaGetDevice(&ctx->device) != cudaSuccess) {
+        cudaGetLastError();
+        delete ctx;
+        return HISS_E_CUDA;
+    }
+    ctx->stream = static_cast<cudaStream_t>(cuda_stream);
+    for (auto &e : ctx->ev) {
+        if (cudaEventCreate(&e) != cudaSuccess) {
+            cudaGetLastError();
+            for (auto &f : ctx->ev)
+                if (f) cudaEventDestroy(f);
+            delete ctx;
+            return HISS_E_CUDA;
+        }
+    }
+    *out = ctx;
+    return HISS_OK;
+}
+
+void hiss_destroy(hiss_ctx *ctx)
+{
+    if (!ctx) return;
+    cudaSetDevice(ctx->device);
+    cudaStreamSynchronize(ctx->stream);
+    DBuf *all[] = {&ctx->x_stage, &ctx->xv, &ctx->perm_d, &ctx->stats_partial, &ctx->stats_out, &ctx->flags,
+                   &ctx->keys, &ctx->vals, &ctx->keys_alt, &ctx->vals_alt, &ctx->sort_tmp, &ctx->xs, &ctx->ids,
+                   &ctx->flag, &ctx->flag_scan, &ctx->cell_start, &ctx->cell_key, &ctx->cell_of_row, &ctx->nbr,
+                   &ctx->nbr_cnt, &ctx->bound, &ctx->work_key, &ctx->cell_idx, &ctx->work, &ctx->scan_tmp,
+                   &ctx->sums2, &ctx->lpt_keys, &ctx->lpt_order, &ctx->ntiles, &ctx->tile_off, &ctx->tile_cell,
+                   &ctx->tile_q0, &ctx->tile_nq, &ctx->tile_word, &ctx->tile_unit, &ctx->tile_qoff,
+                   &ctx->boundaries, &ctx->binfo, &ctx->nb_d, &ctx->mask, &ctx->qcount, &ctx->row_ptr, &ctx->cols,
+                   &ctx->query_ids, &ctx->query_rows, &ctx->cand, &ctx->mask_row_ptr, &ctx->t_keys_alt,
+                   &ctx->t_vals_alt, &ctx->t_sort_tmp, &ctx->t_scan_tmp};
+    for (DBuf *b : all) release(ctx, *b);
+    cudaStreamSynchronize(ctx->stream);
+    if (ctx->h_pinned) cudaFreeHost(ctx->h_pinned);
+    for (auto &e : ctx->ev)
+        if (e) cudaEventDestroy(e);
+    cudaGetLastError();
+    delete ctx;
+}
+
+int hiss_build(hiss_ctx *ctx, const float *d_points, int64_t n, int32_t d)
+{
+    ST(enter(ctx));
+    if (!d_points || n < 1 || n >= (int64_t(1) << 30) || d < 1 || d > HISS_MAX_DIM) return HISS_E_ARG;
+    return do_build(ctx, d_points, n, d);
+}
+
+int hiss_build_host(hiss_ctx *ctx, const float *h_points, int64_t n, int32_t d)
+{
+    ST(enter(ctx));
+    if (!h_points || n < 1 || n >= (int64_t(1) << 30) || d < 1 || d > HISS_MAX_DIM) return HISS_E_ARG;
+    ST(ensure(ctx, ctx->x_stage, sizeof(float) * (size_t)n * d));
+    CK(cudaMemcpyAsync(ctx->x_stage.p, h_points, sizeof(float) * (size_t)n * d, cudaMemcpyHostToDevice,
+                       ctx->stream));
+    return do_build(ctx, as<float>(ctx->x_stage), n, d);
+}
+
+int hiss_count(hiss_ctx *ctx, float eps, int64_t *d_counts)
+{
+    ST(enter(ctx));
+    if (!ctx->built) return HISS_E_STATE;
+    const int64_t launches0 = ctx->launches;
+    ctx->st.ms_index = 0.0;
+    ST(ensure_grid(ctx, eps));
+    CK(cudaEventRecord(ctx->ev[2], ctx->stream));
+    if (d_counts)
+        CK(scatter_counts(as<int32_t>(ctx->ids), as<int32_t>(ctx->cell_of_row), as<int64_t>(ctx->bound), ctx->n,
+                          d_counts, ctx->stream, &ctx->launches));
+    CK(cudaEventRecord(ctx->ev[3], ctx->stream));
+    ST(sync(ctx));
+    fill_grid_stats(ctx);
+    ctx->st.ms_count = elapsed(ctx, 2, 3);
+    ctx->st.kernel_launches = ctx->launches - launches0;
+    return HISS_OK;
+}
+
+int hiss_join(hiss_ctx *ctx, float eps, size_t batch_bytes, const hiss_out *out)
+{
+    ST(enter(ctx));
+    if (!ctx->built) return HISS_E_STATE;
+    if (!(eps >= 0.0f) || std::isinf(eps)) return HISS_E_ARG;
+    return do_join(ctx, eps, batch_bytes, out);
+}
+
+int hiss_index(hiss_ctx *ctx, hiss_index_view *v)
+{
+    ST(enter(ctx));
+    if (!v) return HISS_E_ARG;
+    if (!ctx->grid_valid) return HISS_E_STATE;
+    memset(v, 0, sizeof(*v));
+    v->n = ctx->n;
+    v->cells = ctx->C;
+    v->ids = as<int32_t>(ctx->ids);
+    v->cell_start = as<int32_t>(ctx->cell_start);
+    v->cell_of_row = as<int32_t>(ctx->cell_of_row);
+    v->nbr = as<int32_t>(ctx->nbr);
+    v->nbr_count = as<int32_t>(ctx->nbr_cnt);
+    v->cell_bound = as<int64_t>(ctx->bound);
+    v->cell_key = as<uint64_t>(ctx->cell_key);
+    for (int k = 0; k < 3; ++k) {
+        v->perm[k] = k < ctx->gp.ndim ? ctx->perm[k] : -1;
+        v->origin[k] = ctx->gp.origin[k];
+    }
+    v->sub_bits = ctx->gp.sub_bits;
+    v->cell_width = ctx->gp.w;
+    return HISS_OK;
+}
+
+int hiss_last_stats(const hiss_ctx *ctx, hiss_stats *out)
+{
+    if (!ctx || !out) return HISS_E_ARG;
+    *out = ctx->st;
+    return HISS_OK;
+}
+
+int64_t hiss_launch_count(const hiss_ctx *ctx) { return ctx ? ctx->launches : 0; }
+
+const char *hiss_strerror(int status)
+{
+    switch (status) {
+    case HISS_OK: return "ok";
+    case HISS_E_ARG: return "invalid argument";
+    case HISS_E_NOMEM: return "out of memory";
+    case HISS_E_STATE: return "call out of order or context in error state";
+    case HISS_E_BATCH_TOO_SMALL: return "batch_bytes smaller than one query tile's result mask";
+    case HISS_E_OVERFLOW: return "integer overflow";
+    case HISS_E_CUDA: return "CUDA error";
+    case HISS_E_CALLBACK: return "batch callback requested stop";
+    default: return "unknown status";
+    }
+}
+
+const char *hiss_last_cuda_error(const hiss_ctx *ctx) { return ctx ? ctx->cuda_err : ""; }
+
+int hiss_set_option(hiss_ctx *ctx, int option, int64_t value)
+{
+    if (!ctx) return HISS_E_ARG;
+    if (option == HISS_OPT_ALLOC_LIMIT) {
+        if (value < 0) return HISS_E_ARG;
+        ctx->alloc_limit = value;
+        return HISS_OK;
+    }
+    return HISS_E_ARG;
+}
+
+int hiss_sort_pairs(hiss_ctx *ctx, uint64_t *d_keys, uint32_t *d_vals, int64_t n, int32_t key_bits)
+{
+    ST(enter(ctx));
+    if (!d_keys || !d_vals || n < 0 || n >= (int64_t(1) << 30) || key_bits < 1 || key_bits > 64) return HISS_E_ARG;
+    if (n <= 1) return HISS_OK;
+    ST(ensure(ctx, ctx->t_keys_alt, 8 * (size_t)n));
+    ST(ensure(ctx, ctx->t_vals_alt, 4 * (size_t)n));
+    ST(ensure(ctx, ctx->t_sort_tmp, sort_tmp_bytes(n)));
+    ST(ensure(ctx, ctx->flags, sizeof(int) * kNumFlags * 2));
+    CK(cudaMemsetAsync(ctx->flags.p, 0, sizeof(int) * kNumFlags, ctx->stream));
+    int in_alt = 0;
+    CK(sort_pairs(d_keys, d_vals, as<uint64_t>(ctx->t_keys_alt), as<uint32_t>(ctx->t_vals_alt), n, key_bits,
+                  ctx->t_sort_tmp.p, as<int>(ctx->flags), ctx->stream, &ctx->launches, &in_alt));
+    if (in_alt) {
+        CK(cudaMemcpyAsync(d_keys, ctx->t_keys_alt.p, 8 * (size_t)n, cudaMemcpyDeviceToDevice, ctx->stream));
+        CK(cudaMemcpyAsync(d_vals, ctx->t_vals_alt.p, 4 * (size_t)n, cudaMemcpyDeviceToDevice, ctx->stream));
+    }
+    return check_flags(ctx);
+}
+
+int hiss_exclusive_scan(hiss_ctx *ctx, const int64_t *d_in, int64_t *d_out, int64_t n)
+{
+    ST(enter(ctx));
+    if ((n > 0 && !d_in) || !d_out || n < 0) return HISS_E_ARG;
+    ST(ensure(ctx, ctx->t_scan_tmp, 8 * (size_t)scan_tmp_elems(n + 1) + 64));
+    CK(scan_i64(d_in, d_out, n, as<int64_t>(ctx->t_scan_tmp), ctx->stream, &ctx->launches));
+    return sync(ctx);
+}
+
+int hiss_mask_positions(hiss_ctx *ctx, const uint32_t *d_words, int64_t nbits, int64_t *d_pos, int64_t *h_count)
+{
+    ST(enter(ctx));
+    if (!d_words || !d_pos || !h_count || nbits < 0) return HISS_E_ARG;
+    const int64_t nw = (nbits + 31) >> 5;
+    ST(ensure(ctx, ctx->t_scan_tmp, 8 * (size_t)((nw + 1) / 2 + 1 + nw + 1 + scan_tmp_elems(nw + 1)) + 64));
+    ST(ensure(ctx, ctx->nb_d, 64));
+    CK(mask_positions(d_words, nbits, d_pos, as<int64_t>(ctx->nb_d), as<int64_t>(ctx->t_scan_tmp), ctx->stream,
+                      &ctx->launches));
+    CK(cudaMemcpyAsync(h_count, ctx->nb_d.p, 8, cudaMemcpyDeviceToHost, ctx->stream));
+    return sync(ctx);
+}
+
+}  // extern "C"

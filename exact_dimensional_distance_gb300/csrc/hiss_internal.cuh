@@ -1,0 +1,137 @@
+// Internal declarations shared by the translation units of libhiss.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "hiss.h"
+
+namespace hiss {
+
+// ---- tiling of the refinement kernel ---------------------------------------
+// A refinement unit is one query tile (up to TQ queries of one cell) against
+// one chunk of up to kChunkTiles * TP of the cell's stencil candidates.
+constexpr int kThreads = 256;
+constexpr int kChunkTiles = 64;
+constexpr int kStencil = 27;
+
+// Device-side error flags (one int each in ctx->d_flags).
+enum { kFlagSortTimeout = 0, kFlagPlanTooSmall = 1, kFlagOverflow = 2, kNumFlags = 4 };
+
+// Sticky-error launch check used by every host wrapper.
+#define HISS_TRY(expr)                                      \
+    do {                                                    \
+        cudaError_t e_ = (expr);                            \
+        if (e_ != cudaSuccess) return e_;                   \
+    } while (0)
+
+// ---- scan (scan.cu) --------------------------------------------------------
+// Exclusive prefix sums; out has n + 1 entries (out[n] = total).  tmp must
+// hold scan_tmp_elems(n) int64 values.  in and out may alias for the
+// int64 -> int64 form.
+int64_t scan_tmp_elems(int64_t n);
+cudaError_t scan_i64(const int64_t *in, int64_t *out, int64_t n, int64_t *tmp, cudaStream_t s, int64_t *launches);
+cudaError_t scan_i32_to_i64(const int32_t *in, int64_t *out, int64_t n, int64_t *tmp, cudaStream_t s, int64_t *launches);
+cudaError_t scan_i32(const int32_t *in, int32_t *out, int64_t n, int64_t *tmp, cudaStream_t s, int64_t *launches);
+
+// ---- onesweep radix sort (sort.cu) -----------------------------------------
+size_t sort_tmp_bytes(int64_t n);
+// Sorts (keys, vals) by the low key_bits bits.  keys_alt/vals_alt are
+// ping-pong buffers of n entries.  On return *in_alt tells whether the
+// sorted data are in the alt buffers.  flags: device int[kNumFlags].
+cudaError_t sort_pairs(uint64_t *keys, uint32_t *vals, uint64_t *keys_alt, uint32_t *vals_alt, int64_t n,
+                       int key_bits, void *tmp, int *flags, cudaStream_t s, int64_t *launches, int *in_alt);
+
+// ---- index kernels (index.cu) ----------------------------------------------
+int64_t stats_blocks(int64_t n, int d);
+// partial: [blocks][d][4] doubles; out: [4][d] doubles (min, max, mean, var)
+// and nonfinite: device int (count of non-finite inputs).
+cudaError_t dim_stats(const float *x, int64_t n, int d, double *partial, double *out, int *nonfinite,
+                      cudaStream_t s, int64_t *launches);
+cudaError_t permute_pad(const float *x, int64_t n, int d, int d4, const int32_t *perm, float *xv,
+                        cudaStream_t s, int64_t *launches);
+
+struct GridParams {
+    double origin[3];
+    double w;
+    int sub_bits;
+    int key_bits;
+    int ndim;  // index dimensions used (min(d, 3))
+};
+cudaError_t cell_keys(const float *xv, int64_t n, int d4, GridParams gp, uint64_t *keys, uint32_t *vals,
+                      cudaStream_t s, int64_t *launches);
+cudaError_t gather_rows(const float *xv, const uint32_t *order, int64_t n, int d4, float *xs, int32_t *ids,
+                        cudaStream_t s, int64_t *launches);
+cudaError_t cell_flags(const uint64_t *keys, int64_t n, int shift, int32_t *flag, cudaStream_t s, int64_t *launches);
+cudaError_t cell_starts(const uint64_t *keys, const int32_t *flag_scan, int64_t n, int shift, int32_t *cell_start,
+                        uint64_t *cell_key, int32_t *cell_of_row, cudaStream_t s, int64_t *launches);
+cudaError_t stencil(const uint64_t *cell_key, const int32_t *cell_start, int64_t C, int32_t *nbr, int32_t *nbr_cnt,
+                    int64_t *bound, uint64_t *work_key, uint32_t *cell_idx, int64_t *work, cudaStream_t s,
+                    int64_t *launches);
+cudaError_t scatter_counts(const int32_t *ids, const int32_t *cell_of_row, const int64_t *bound, int64_t n,
+                           int64_t *counts, cudaStream_t s, int64_t *launches);
+// Per cell in processing order: tiles and their sizes.
+cudaError_t tile_counts(const uint32_t *order, const int32_t *cell_start, int64_t C, int tq, int32_t *ntiles,
+                        cudaStream_t s, int64_t *launches);
+cudaError_t tile_fill(const uint32_t *order, const int32_t *cell_start, const int64_t *bound,
+                      const int64_t *tile_off, int64_t C, int tq, int chunk, int32_t *tile_cell, int32_t *tile_q0,
+                      int32_t *tile_nq, int64_t *tile_words, int64_t *tile_units, cudaStream_t s,
+                      int64_t *launches);
+// Greedy batches over query tiles: boundaries[k] = first tile of batch k,
+// boundaries[nb] = T; *nb written to nb_out (device).  info[4 k + 0..2] =
+// (word offset, unit offset, query offset) at boundary k, for k = 0..nb.
+// flags[kFlagPlanTooSmall] is set when one tile's mask exceeds cap_words.
+cudaError_t plan_batches(const int64_t *tile_word_off, const int64_t *tile_unit, const int64_t *tile_qoff,
+                         int64_t T, int64_t cap_words, int64_t *boundaries, int64_t *info, int64_t *nb_out,
+                         int *flags, cudaStream_t s, int64_t *launches);
+
+// ---- refinement and compaction (refine.cu) ---------------------------------
+struct RefineArgs {
+    const float *xs;            // index-ordered points, n x d4 (row stride d4)
+    const int32_t *cell_start;  // [C+1]
+    const int32_t *nbr;         // [C*27]
+    const int32_t *nbr_cnt;     // [C]
+    const int64_t *bound;       // [C]
+    const int32_t *tile_cell;   // [T]
+    const int32_t *tile_q0;     // [T] first index row of the tile
+    const int32_t *tile_nq;     // [T]
+    const int64_t *tile_word;   // [T+1] mask word offset (absolute)
+    const int64_t *tile_unit;   // [T+1] first unit of each tile (absolute)
+    const int64_t *tile_qoff;   // [T+1] first query (absolute, processing order)
+    int64_t t0, t1;             // batch: tiles [t0, t1)
+    int64_t unit0, nunits;      // units of the batch
+    int64_t word0, q0;          // batch origin in words and queries
+    uint32_t *mask;             // batch mask
+    int32_t *qcount;            // [nq of batch] neighbour count per query (accumulated)
+    int d4;
+    float eps2;
+};
+int refine_tq(int d4);
+int refine_chunk(int d4);
+cudaError_t refine(const RefineArgs &a, cudaStream_t s, int64_t *launches);
+
+struct CompactArgs {
+    const int32_t *ids;         // [n] original id per index row
+    const int32_t *cell_start;
+    const int32_t *nbr;
+    const int32_t *nbr_cnt;
+    const int64_t *bound;
+    const int32_t *tile_cell;
+    const int32_t *tile_q0;
+    const int64_t *tile_word;
+    const int64_t *tile_qoff;
+    int64_t t0, t1, word0, q0, nq;
+    const uint32_t *mask;
+    const int64_t *row_ptr;     // [nq+1] batch-relative
+    int32_t *cols;              // CSR output (NULL: only query ids/rows/cand)
+    int64_t *query_ids;         // [nq]
+    int32_t *query_rows;        // [nq]
+    int64_t *cand;              // [nq] B_q (may be NULL)
+    int64_t *mask_row_ptr;      // [nq+1] word offsets (may be NULL)
+};
+cudaError_t compact(const CompactArgs &a, cudaStream_t s, int64_t *launches);
+cudaError_t mask_positions(const uint32_t *words, int64_t nbits, int64_t *pos, int64_t *count,
+                           int64_t *tmp, cudaStream_t s, int64_t *launches);
+
+}  // namespace hiss

@@ -1,0 +1,367 @@
+// Candidate refinement on CUDA cores (RT-HiSS Section IV-E) and stream
+// compaction of the result mask (Section IV-F1, Fig. 5).
+//
+// One thread block refines one unit: a tile of up to TQ queries of one grid
+// cell against one chunk of the cell's stencil candidates (the cells around
+// it, concatenated in stencil order).  The query tile stays in shared memory;
+// candidate tiles of TP points are staged through shared memory with cp.async,
+// double-buffered, gathered row by row from the stencil cells.  Each thread
+// owns an MQ x MP block of (query, candidate) squared distances in registers
+// and adds four dimensions per step (one 16-byte shared load per point), so
+// a step costs 2 * MQ * MP * 4 FP32 instructions against MQ + MP loads.
+// Dimensions are in variance order, so every eight dimensions a warp checks
+// whether all of its partial sums already exceed eps^2 and, if so, skips the
+// rest of the tile (early termination, Section IV-A).  The result is one bit
+// per pair, sum <= eps^2, written to the query's mask row; the popcount of each
+// word is accumulated into the query's neighbour count.
+#include "hiss_internal.cuh"
+
+namespace hiss {
+namespace {
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
+{
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+// Row stride of a staged tile, in floats: d4 plus padding chosen so that
+// stride / 4 is odd, which makes the 16-byte loads of 8 consecutive rows hit
+// 8 distinct bank quads.
+__host__ __device__ __forceinline__ int tile_stride(int d4) { return ((d4 / 4) % 2 == 0) ? d4 + 4 : d4 + 8; }
+
+template <int MQ, int MP>
+struct Tile {
+    static constexpr int TQ = 16 * MQ;   // 4 warps x 4 lanes x MQ queries
+    static constexpr int TP = 16 * MP;   // 2 warps x 8 lanes x MP candidates
+    static constexpr int CH = kChunkTiles * TP;
+    static constexpr int WPW = MP / 4;   // mask words per query per warp column
+};
+
+template <int MQ, int MP>
+__global__ void __launch_bounds__(kThreads, 1) k_refine(const RefineArgs a)
+{
+    using T = Tile<MQ, MP>;
+    extern __shared__ __align__(16) float smem[];
+    __shared__ int32_t s_nstart[kStencil];
+    __shared__ int32_t s_vpre[kStencil + 1];
+    __shared__ int64_t s_info[8];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int d4 = a.d4, S = tile_stride(d4), C4 = d4 / 4;
+    float *Qs = smem;
+    float *Ps0 = smem + T::TQ * S;
+
+    if (tid == 0) {
+        const int64_t u = a.unit0 + blockIdx.x;
+        int64_t lo = a.t0, hi = a.t1 - 1;  // last tile with tile_unit[t] <= u
+        while (lo < hi) {
+            const int64_t mid = (lo + hi + 1) >> 1;
+            if (a.tile_unit[mid] <= u) lo = mid; else hi = mid - 1;
+        }
+        s_info[0] = lo;
+        s_info[1] = u - a.tile_unit[lo];
+    }
+    __syncthreads();
+    const int64_t t = s_info[0];
+    const int64_t chunk = s_info[1];
+    const int32_t c = a.tile_cell[t];
+    const int32_t q0 = a.tile_q0[t];
+    const int nq = a.tile_nq[t];
+    const int64_t B = a.bound[c];
+    const int64_t W = (B + 31) >> 5;
+    const int ns = a.nbr_cnt[c];
+    if (tid < ns) {
+        const int32_t nb = a.nbr[(int64_t)c * kStencil + tid];
+        s_nstart[tid] = a.cell_start[nb];
+        s_vpre[tid + 1] = a.cell_start[nb + 1] - a.cell_start[nb];
+    }
+    __syncthreads();
+    if (tid == 0) {
+        s_vpre[0] = 0;
+        for (int i = 1; i <= ns; ++i) s_vpre[i] += s_vpre[i - 1];
+    }
+
+    // query tile: rows q0 .. q0+nq, +inf beyond
+    for (int idx = tid; idx < T::TQ * C4; idx += kThreads) {
+        const int r = idx / C4, cc = idx - r * C4;
+        float *dst = Qs + r * S + 4 * cc;
+        if (r < nq) cp_async16(dst, a.xs + (int64_t)(q0 + r) * d4 + 4 * cc);
+        else *reinterpret_cast<float4 *>(dst) = make_float4(INFINITY, INFINITY, INFINITY, INFINITY);
+    }
+    __syncthreads();  // s_vpre complete
+
+    const int64_t vbeg = chunk * T::CH;
+    const int64_t vend = min(B, vbeg + (int64_t)T::CH);
+    const int ntiles = (int)((vend - vbeg + T::TP - 1) / T::TP);
+
+    auto load_p = [&](int buf, int64_t v0) {
+        float *P = Ps0 + buf * T::TP * S;
+        for (int idx = tid; idx < T::TP * C4; idx += kThreads) {
+            const int r = idx / C4, cc = idx - r * C4;
+            float *dst = P + r * S + 4 * cc;
+            const int64_t v = v0 + r;
+            if (v < vend) {
+                int lo = 0, hi = ns - 1;  // last slot with s_vpre[slot] <= v
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (s_vpre[mid] <= v) lo = mid; else hi = mid - 1;
+                }
+                const int64_t src = s_nstart[lo] + (v - s_vpre[lo]);
+                cp_async16(dst, a.xs + src * d4 + 4 * cc);
+            } else {
+                *reinterpret_cast<float4 *>(dst) = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+        }
+    };
+
+    load_p(0, vbeg);
+    cp_async_commit();
+
+    const int wq = warp >> 1, wp = warp & 1;
+    const int lq = lane >> 3, lp = lane & 7;
+    const int qbase = wq * (4 * MQ) + lq;  // query row j: qbase + 4 j
+    const int pbase = wp * (8 * MP) + lp;  // candidate row j: pbase + 8 j
+    const float eps2 = a.eps2;
+    uint32_t my_count = 0;                 // neighbours of query row qbase + 4 lp (lp < MQ)
+    const int64_t row_word0 = a.tile_word[t] - a.word0;
+
+    for (int it = 0; it < ntiles; ++it) {
+        const int64_t v0 = vbeg + (int64_t)it * T::TP;
+        if (it + 1 < ntiles) {
+            load_p((it + 1) & 1, v0 + T::TP);
+            cp_async_commit();
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+
+        const float *P = Ps0 + (it & 1) * T::TP * S;
+        float acc[MQ][MP];
+#pragma unroll
+        for (int i = 0; i < MQ; ++i)
+#pragma unroll
+            for (int j = 0; j < MP; ++j) acc[i][j] = 0.0f;
+
+        for (int k = 0; k < d4; k += 4) {
+            float4 qv[MQ];
+#pragma unroll
+            for (int i = 0; i < MQ; ++i) qv[i] = *reinterpret_cast<const float4 *>(Qs + (qbase + 4 * i) * S + k);
+#pragma unroll
+            for (int j = 0; j < MP; ++j) {
+                const float4 pv = *reinterpret_cast<const float4 *>(P + (pbase + 8 * j) * S + k);
+#pragma unroll
+                for (int i = 0; i < MQ; ++i) {
+                    float e;
+                    e = qv[i].x - pv.x; acc[i][j] = fmaf(e, e, acc[i][j]);
+                    e = qv[i].y - pv.y; acc[i][j] = fmaf(e, e, acc[i][j]);
+                    e = qv[i].z - pv.z; acc[i][j] = fmaf(e, e, acc[i][j]);
+                    e = qv[i].w - pv.w; acc[i][j] = fmaf(e, e, acc[i][j]);
+                }
+            }
+            if (((k + 4) & 7) == 0 && k + 4 < d4) {
+                float m = acc[0][0];
+#pragma unroll
+                for (int i = 0; i < MQ; ++i)
+#pragma unroll
+                    for (int j = 0; j < MP; ++j) m = fminf(m, acc[i][j]);
+                if (__all_sync(0xffffffffu, m > eps2)) break;
+            }
+        }
+
+        // one bit per pair; OR across the 8 lanes of a query row; lane lp
+        // writes the words of query j = lp
+        const int64_t word_tile = v0 >> 5;
+#pragma unroll
+        for (int i = 0; i < MQ; ++i) {
+#pragma unroll
+            for (int wi = 0; wi < T::WPW; ++wi) {
+                uint32_t w = 0;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    w |= (acc[i][4 * wi + jj] <= eps2 ? 1u : 0u) << (lp + 8 * jj);
+                w |= __shfl_xor_sync(0xffffffffu, w, 1);
+                w |= __shfl_xor_sync(0xffffffffu, w, 2);
+                w |= __shfl_xor_sync(0xffffffffu, w, 4);
+                const int qr = qbase + 4 * i;
+                const int64_t wcol = word_tile + wp * T::WPW + wi;
+                if (lp == i && qr < nq && wcol < W) {
+                    a.mask[row_word0 + (int64_t)qr * W + wcol] = w;
+                    my_count += __popc(w);
+                }
+            }
+        }
+        __syncthreads();
+    }
+    if (lp < MQ) {
+        const int qr = qbase + 4 * lp;
+        if (qr < nq && my_count) atomicAdd(&a.qcount[a.tile_qoff[t] - a.q0 + qr], (int32_t)my_count);
+    }
+}
+
+template <int MQ, int MP>
+cudaError_t launch_refine(const RefineArgs &a, cudaStream_t s)
+{
+    using T = Tile<MQ, MP>;
+    const size_t smem = sizeof(float) * (size_t)(T::TQ + 2 * T::TP) * tile_stride(a.d4);
+    static size_t configured = 0;  // largest dynamic shared memory requested so far
+    if (smem > configured) {
+        HISS_TRY(cudaFuncSetAttribute(k_refine<MQ, MP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        configured = smem;
+    }
+    if (a.nunits <= 0) return cudaSuccess;
+    k_refine<MQ, MP><<<(unsigned)a.nunits, kThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+// ---- compaction: one warp per query row --------------------------------------
+constexpr int kCompactWarps = 8;
+
+__global__ void __launch_bounds__(kCompactWarps * 32) k_compact(const CompactArgs a)
+{
+    __shared__ int32_t s_start[kCompactWarps][kStencil];
+    __shared__ int32_t s_vpre[kCompactWarps][kStencil + 1];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t gq = (int64_t)blockIdx.x * kCompactWarps + warp;
+    if (gq >= a.nq) return;
+    const int64_t qa = a.q0 + gq;
+    int64_t lo = a.t0, hi = a.t1 - 1;  // last tile with tile_qoff[t] <= qa
+    while (lo < hi) {
+        const int64_t mid = (lo + hi + 1) >> 1;
+        if (a.tile_qoff[mid] <= qa) lo = mid; else hi = mid - 1;
+    }
+    const int64_t t = lo;
+    const int64_t i = qa - a.tile_qoff[t];
+    const int32_t c = a.tile_cell[t];
+    const int32_t row = a.tile_q0[t] + (int32_t)i;
+    const int64_t B = a.bound[c];
+    const int64_t W = (B + 31) >> 5;
+    const int64_t woff = a.tile_word[t] - a.word0 + i * W;
+    if (lane == 0) {
+        a.query_ids[gq] = a.ids[row];
+        a.query_rows[gq] = row;
+        if (a.cand) a.cand[gq] = B;
+        if (a.mask_row_ptr) {
+            a.mask_row_ptr[gq] = woff;
+            if (gq == a.nq - 1) a.mask_row_ptr[a.nq] = woff + W;
+        }
+    }
+    if (!a.cols) return;
+    const int ns = a.nbr_cnt[c];
+    int32_t sz = 0;
+    if (lane < ns) {
+        const int32_t nb = a.nbr[(int64_t)c * kStencil + lane];
+        s_start[warp][lane] = a.cell_start[nb];
+        sz = a.cell_start[nb + 1] - a.cell_start[nb];
+    }
+    int32_t incl = sz;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane < ns) s_vpre[warp][lane] = incl - sz;
+    __syncwarp();
+
+    const uint32_t *mrow = a.mask + woff;
+    int32_t *out = a.cols + a.row_ptr[gq];
+    int64_t run = 0;
+    for (int64_t w0 = 0; w0 < W; w0 += 32) {
+        const int64_t w = w0 + lane;
+        uint32_t word = w < W ? mrow[w] : 0u;
+        const int cnt = __popc(word);
+        int ex = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, ex, o);
+            if (lane >= o) ex += v;
+        }
+        const int total = __shfl_sync(0xffffffffu, ex, 31);
+        int64_t pos = run + ex - cnt;
+        while (word) {
+            const int b = __ffs(word) - 1;
+            word &= word - 1;
+            const int64_t v = w * 32 + b;
+            int l = 0, h = ns - 1;
+            while (l < h) {
+                const int m = (l + h + 1) >> 1;
+                if (s_vpre[warp][m] <= v) l = m; else h = m - 1;
+            }
+            out[pos++] = a.ids[s_start[warp][l] + (v - s_vpre[warp][l])];
+        }
+        run += total;
+    }
+}
+
+__global__ void k_word_popc(const uint32_t *words, int64_t nbits, int32_t *cnt)
+{
+    const int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nw = (nbits + 31) >> 5;
+    if (w >= nw) return;
+    uint32_t x = words[w];
+    const int64_t rem = nbits - w * 32;
+    if (rem < 32) x &= (1u << rem) - 1u;
+    cnt[w] = __popc(x);
+}
+
+__global__ void k_word_positions(const uint32_t *words, int64_t nbits, const int64_t *off, int64_t *pos)
+{
+    const int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nw = (nbits + 31) >> 5;
+    if (w >= nw) return;
+    uint32_t x = words[w];
+    const int64_t rem = nbits - w * 32;
+    if (rem < 32) x &= (1u << rem) - 1u;
+    int64_t o = off[w];
+    while (x) {
+        const int b = __ffs(x) - 1;
+        x &= x - 1;
+        pos[o++] = w * 32 + b;
+    }
+}
+
+}  // namespace
+
+int refine_tq(int d4) { return d4 <= 128 ? Tile<8, 8>::TQ : Tile<4, 4>::TQ; }
+
+cudaError_t refine(const RefineArgs &a, cudaStream_t s, int64_t *launches)
+{
+    ++*launches;
+    if (a.d4 <= 128) return launch_refine<8, 8>(a, s);
+    return launch_refine<4, 4>(a, s);
+}
+
+int refine_chunk(int d4) { return d4 <= 128 ? Tile<8, 8>::CH : Tile<4, 4>::CH; }
+
+cudaError_t compact(const CompactArgs &a, cudaStream_t s, int64_t *launches)
+{
+    if (a.nq <= 0) return cudaSuccess;
+    const int64_t blocks = (a.nq + kCompactWarps - 1) / kCompactWarps;
+    k_compact<<<(unsigned)blocks, kCompactWarps * 32, 0, s>>>(a);
+    ++*launches;
+    return cudaGetLastError();
+}
+
+cudaError_t mask_positions(const uint32_t *words, int64_t nbits, int64_t *pos, int64_t *count, int64_t *tmp,
+                           cudaStream_t s, int64_t *launches)
+{
+    // tmp: [nw] int32 counts, then [nw+1] int64 offsets, then scan scratch
+    const int64_t nw = (nbits + 31) >> 5;
+    int32_t *cnt = reinterpret_cast<int32_t *>(tmp);
+    int64_t *off = tmp + (nw + 1) / 2 + 1;
+    int64_t *scratch = off + nw + 1;
+    const unsigned blocks = (unsigned)((nw + 255) / 256);
+    if (nw == 0) return cudaMemsetAsync(count, 0, sizeof(int64_t), s);
+    k_word_popc<<<blocks, 256, 0, s>>>(words, nbits, cnt);
+    HISS_TRY(scan_i32_to_i64(cnt, off, nw, scratch, s, launches));
+    k_word_positions<<<blocks, 256, 0, s>>>(words, nbits, off, pos);
+    *launches += 2;
+    HISS_TRY(cudaMemcpyAsync(count, off + nw, sizeof(int64_t), cudaMemcpyDeviceToDevice, s));
+    return cudaGetLastError();
+}
+
+}  // namespace hiss

@@ -1,0 +1,224 @@
+/*
+ * hiss.h -- C ABI of the GB300 exact epsilon self-join library (libhiss.so).
+ *
+ * The operation (RT-HiSS, Munugala & Gowanlock, "RT-HiSS: Ray Tracing
+ * Accelerated High Dimensional Vector Similarity Searches", Section II-A,
+ * "Problem Statement"): for a dataset D of n points in R^d, return every pair
+ * (i, j) with Euclidean distance dist(p_i, p_j) <= eps, inclusive; each point
+ * is its own neighbour.  The library computes it in the three steps of the
+ * paper's Section IV, rebuilt for one GPU without ray-tracing cores:
+ *
+ *   hiss_build  -- per-dimension variance and the variance order of the
+ *                  dimensions (Section IV-A); the data are kept on the device
+ *                  in that order.
+ *   hiss_count  -- a three-dimensional grid over the three highest-variance
+ *                  dimensions (grid indexing, Section II-B1) with Morton-ordered
+ *                  points (Section IV-C), and the count pass that bounds every
+ *                  query's candidate count (first intersection test and pass 1,
+ *                  Section IV-D).
+ *   hiss_join   -- batches sized from the count pass (Section IV-D), exact
+ *                  refinement on CUDA cores with shared-memory tiling and early
+ *                  termination in variance order (Sections IV-A and IV-E), a
+ *                  one-bit-per-candidate result mask and its stream compaction
+ *                  (Section IV-F1, Fig. 5), and optional delivery to host memory
+ *                  (Section IV-F2).
+ *
+ * Conventions shared by every call
+ *   - Every call returns HISS_OK (0) or a negative hiss_status; none aborts.
+ *     A CUDA error inside the library is sticky: the call that meets it
+ *     returns HISS_E_CUDA and every later call on the context returns
+ *     HISS_E_STATE (destroy the context and create a new one).
+ *   - "device pointer" means memory of the current CUDA device (cudaMalloc,
+ *     a torch CUDA tensor, ...); "host pointer" means ordinary or pinned host
+ *     memory.  The library never frees memory it did not allocate.
+ *   - A context is bound to the CUDA stream given at creation and to the
+ *     device current at that time.  All device work of a call is ordered on
+ *     that stream; calls return after the work they describe is complete
+ *     unless stated otherwise.  A context is not thread-safe.
+ *   - Point ids are the row indices of the array given to hiss_build
+ *     (0-based).  n must be below 2^30 and d at most HISS_MAX_DIM.
+ */
+#ifndef HISS_H
+#define HISS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define HISS_MAX_DIM 256
+
+typedef enum {
+    HISS_OK = 0,
+    HISS_E_ARG = -1,             /* invalid argument (NULL, n < 1, d out of range, eps < 0 or NaN, non-finite input) */
+    HISS_E_NOMEM = -2,           /* a device or pinned allocation failed (or exceeded the allocation limit) */
+    HISS_E_STATE = -3,           /* call out of order (join before build), or the context holds a sticky CUDA error */
+    HISS_E_BATCH_TOO_SMALL = -4, /* batch_bytes is smaller than the result mask of one query tile */
+    HISS_E_OVERFLOW = -5,        /* a count exceeded the library's integer ranges */
+    HISS_E_CUDA = -6,            /* a CUDA runtime call or kernel failed; see hiss_last_cuda_error */
+    HISS_E_CALLBACK = -7         /* the batch callback returned non-zero; the join stopped */
+} hiss_status;
+
+typedef struct hiss_ctx hiss_ctx;
+
+/* Create a context on the current CUDA device.  cuda_stream is a
+ * cudaStream_t (NULL = the legacy default stream).  The context owns every
+ * internal device buffer; none is allocated before the first build. */
+int hiss_create(hiss_ctx **out, void *cuda_stream);
+
+/* Free every resource of the context.  NULL is ignored. */
+void hiss_destroy(hiss_ctx *ctx);
+
+/* Load the dataset.  d_points: device pointer to n x d float32, row-major
+ * (row i = point i), read only during the call; the library keeps its own
+ * copy, so the caller may free or overwrite the array afterwards.  Computes
+ * the per-dimension min, max and variance (fp64 accumulation) and the
+ * variance order of the dimensions, descending, equal variances by lower
+ * index (RT-HiSS Section IV-A), and stores the points with their dimensions in
+ * that order, padded with zeros to a multiple of 4.  Rejects non-finite
+ * coordinates with HISS_E_ARG.  Discards any index built for an earlier
+ * dataset. */
+int hiss_build(hiss_ctx *ctx, const float *d_points, int64_t n, int32_t d);
+
+/* As hiss_build, with h_points a host pointer; the copy to the device is part
+ * of the call. */
+int hiss_build_host(hiss_ctx *ctx, const float *h_points, int64_t n, int32_t d);
+
+/* Build the grid index for eps (reused while eps is unchanged) and write the
+ * count bound of every point: d_counts (device pointer, int64[n], original
+ * point order; may be NULL to build the index only) receives B_q, the number
+ * of points in the 27 grid cells around q's cell, q's own cell included.
+ * B_q >= |{j : dist(q, p_j) <= eps}| for every q (the grid cell side exceeds
+ * eps).  This is the per-query intersection count of the first intersection
+ * test (RT-HiSS Section IV-D) for the grid index.  eps must be finite and
+ * >= 0. */
+int hiss_count(hiss_ctx *ctx, float eps, int64_t *d_counts);
+
+/* One batch of results handed to the caller. */
+typedef struct {
+    int64_t index;              /* batch number, 0-based */
+    int64_t nq;                 /* queries in this batch */
+    const int64_t *query_ids;   /* [nq] original id of each query, in processing order */
+    const int64_t *row_ptr;     /* [nq+1] CSR: offsets into cols; MASK: offsets into mask (32-bit words) */
+    const int32_t *cols;        /* CSR: [nnz] original ids of the neighbours (unordered within a row); else NULL */
+    const uint32_t *mask;       /* MASK: [n_words] result mask; else NULL */
+    const int64_t *cand;        /* MASK: [nq] candidate count B_q (bits used in the row); else NULL */
+    const int32_t *query_rows;  /* [nq] row of each query in the index order (see hiss_index) */
+    int64_t nnz;                /* CSR: pairs in this batch (self pairs included) */
+    int64_t n_words;            /* MASK: mask words in this batch */
+    int32_t on_host;            /* 1: every pointer above is host memory; 0: device memory */
+    int32_t mode;               /* HISS_OUT_CSR or HISS_OUT_MASK */
+} hiss_batch;
+
+/* Called once per batch, in batch order, after the batch is complete on the
+ * device (and copied to the host when copy_to_host = 1).  The pointers are
+ * valid only until the callback returns.  A non-zero return stops the join
+ * with HISS_E_CALLBACK. */
+typedef int (*hiss_batch_fn)(void *user, const hiss_batch *batch);
+
+enum { HISS_OUT_CSR = 0, HISS_OUT_MASK = 1 };
+
+typedef struct {
+    int32_t mode;            /* HISS_OUT_CSR (default) or HISS_OUT_MASK */
+    int32_t copy_to_host;    /* 1: copy each batch to pinned host memory before the callback */
+    hiss_batch_fn on_batch;  /* may be NULL: results are produced on the device and dropped */
+    void *user;              /* passed to on_batch */
+} hiss_out;
+
+/* The self-join for eps.  Builds (or reuses) the grid index of hiss_count,
+ * orders the grid cells by decreasing work |cell| * B_cell so that the
+ * largest work goes first (RT-HiSS Section IV-D), and cuts them, one query
+ * tile at a time, into batches whose result mask (one bit per candidate
+ * pair, ceil(B_q / 32) words per query) fits in batch_bytes.  Each batch is
+ * refined exactly on CUDA cores (float32 squared distances summed in
+ * variance order, pair rejected once the partial sum exceeds eps^2; bit =
+ * sum <= eps^2), compacted from the mask to CSR (Section IV-F1) unless
+ * out->mode is HISS_OUT_MASK, and handed to out->on_batch.  Every query
+ * appears in exactly one batch; every row contains the query itself.
+ * batch_bytes = 0 selects 1/4 of the free device memory.  out may be NULL
+ * (CSR, device, no callback).
+ *
+ * Mask layout (HISS_OUT_MASK): bit v of a query's row (word v / 32, bit
+ * v % 32) is the v-th candidate of the query's cell: the cells of the
+ * stencil in the order given by hiss_index (dz, dy, dx, dz outermost), each
+ * cell's points in index order. */
+int hiss_join(hiss_ctx *ctx, float eps, size_t batch_bytes, const hiss_out *out);
+
+/* Read-only view of the index built for the last eps (device pointers owned
+ * by the context, valid until the next build or a call with another eps). */
+typedef struct {
+    int64_t n;                  /* points */
+    int64_t cells;              /* non-empty grid cells C */
+    const int32_t *ids;         /* [n] original id of the point at each index row (Morton order) */
+    const int32_t *cell_start;  /* [C+1] first index row of each cell; cell_start[C] = n */
+    const int32_t *cell_of_row; /* [n] cell of each index row */
+    const int32_t *nbr;         /* [C*27] existing stencil cells of each cell, first nbr_count[c] used */
+    const int32_t *nbr_count;   /* [C] */
+    const int64_t *cell_bound;  /* [C] B_cell: points in the cell's stencil */
+    const uint64_t *cell_key;   /* [C] Morton key of each cell's grid coordinates */
+    int32_t perm[3];            /* index dimensions (original dimension numbers), highest variance first */
+    int32_t sub_bits;           /* sub-cell bits per dimension used to order points inside a cell */
+    double cell_width;          /* grid cell side w > eps */
+    double origin[3];           /* grid origin on the three index dimensions */
+} hiss_index_view;
+
+int hiss_index(hiss_ctx *ctx, hiss_index_view *out);
+
+/* Counters and timings of the last hiss_count / hiss_join. */
+typedef struct {
+    int64_t n, cells, cell_pairs;   /* points, non-empty cells, stencil cell pairs */
+    int64_t candidates;             /* sum of B_q over all queries (candidate distance evaluations) */
+    int64_t pairs;                  /* result pairs |R| of the last join, self pairs included */
+    int64_t batches, query_tiles, refine_units;
+    int64_t mask_words_max;         /* largest batch mask, 32-bit words */
+    int64_t kernel_launches;        /* kernels launched by the last call */
+    int32_t d, d_pad, sub_bits, key_bits;
+    float eps;
+    double cell_width;
+    double ms_build, ms_index, ms_count, ms_refine, ms_compact, ms_deliver, ms_total;
+} hiss_stats;
+
+int hiss_last_stats(const hiss_ctx *ctx, hiss_stats *out);
+
+/* Kernels launched by this context since creation (all calls). */
+int64_t hiss_launch_count(const hiss_ctx *ctx);
+
+/* Human-readable name of a status code (static string). */
+const char *hiss_strerror(int status);
+
+/* The CUDA error string behind the last HISS_E_CUDA of this context. */
+const char *hiss_last_cuda_error(const hiss_ctx *ctx);
+
+/* Options.  HISS_OPT_ALLOC_LIMIT: cap, in bytes, on the device memory the
+ * context may hold (0 = no cap); an allocation beyond it fails with
+ * HISS_E_NOMEM without calling the CUDA allocator.  Used to test the
+ * out-of-memory path without exhausting the device. */
+enum { HISS_OPT_ALLOC_LIMIT = 1 };
+int hiss_set_option(hiss_ctx *ctx, int option, int64_t value);
+
+/* ---- building blocks exposed for testing ---------------------------------
+ * These run the library's own kernels on caller data (device pointers) on
+ * the context's stream and return when done. */
+
+/* Stable LSD radix sort (onesweep: one digit histogram pass, then one
+ * decoupled-look-back scatter pass per 8-bit digit) of n (key, value) pairs
+ * by the low key_bits bits of the key (1..64); keys and vals are sorted in
+ * place.  n < 2^30. */
+int hiss_sort_pairs(hiss_ctx *ctx, uint64_t *d_keys, uint32_t *d_vals, int64_t n, int32_t key_bits);
+
+/* Exclusive prefix sum of n int64 values: out[i] = sum(in[0..i)), out[n] =
+ * total (out has n + 1 entries).  in and out may alias. */
+int hiss_exclusive_scan(hiss_ctx *ctx, const int64_t *d_in, int64_t *d_out, int64_t n);
+
+/* Stream compaction of one result mask (RT-HiSS Section IV-F1, Fig. 5):
+ * writes the positions of the ones among the first nbits bits of d_words
+ * (bit v = word v / 32, bit v % 32) to d_pos in increasing order and their
+ * number to *h_count (host).  d_pos must hold nbits entries. */
+int hiss_mask_positions(hiss_ctx *ctx, const uint32_t *d_words, int64_t nbits, int64_t *d_pos, int64_t *h_count);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HISS_H */

@@ -176,6 +176,13 @@ def pick_eps(x, k_mean: int, qidx) -> dict:
         m *= 4
     e2 = 0.5 * (a.value + b.value)
     eps = np.float32(np.sqrt(e2))
+    # eps is a float32: keep a <= eps^2 < b when a float32 lies in [sqrt(a), sqrt(b))
+    zero = np.float32(0.0)
+    while eps > 0 and float(eps) * float(eps) >= b.value:
+        eps = np.nextafter(eps, zero)
+    up = np.nextafter(eps, np.float32(np.inf))
+    if float(eps) * float(eps) < a.value and float(up) * float(up) < b.value:
+        eps = up
     return {"eps": float(eps), "eps_hex": float(eps).hex(), "a": a.value, "b": b.value,
             "eps2_mid": e2, "nq": int(q.size), "k": int(k_mean)}
 

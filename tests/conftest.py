@@ -25,3 +25,10 @@ def read_golden(name):
             tag, *vals = line.split()
             rows.append((tag, vals))
     return rows
+
+
+def golden_eps(cfg):
+    """eps of synthetic workload cfg (written by tests/golden/make_eps.py)."""
+    import json
+    with open(os.path.join(GOLDEN, "eps_configs.json")) as f:
+        return json.load(f)[str(cfg)]["eps"]

@@ -4,7 +4,8 @@ Calls only the oracle (fp64 brute force) and the seeded generators.  For
 workload c, 1,000 query indices are drawn without replacement with
 numpy.random.default_rng(1000 + c); eps is the oracle's picker result for the
 workload's target mean neighbour count (self excluded), and the sampled mean
-is re-counted with the float32 eps to confirm it equals the target exactly.
+is re-counted with the float32 eps to confirm it equals the target (exactly
+when a float32 lies between the two order statistics that bracket it).
 
     python tests/golden/make_eps.py [config ...]
 """
@@ -35,7 +36,9 @@ def pick(cfg: int) -> dict:
     sampled_mean = (int(row_ptr[-1]) - q.size) / q.size
     r.update({"config": cfg, "workload": name, "n": n, "d": d, "sample_seed": 1000 + cfg,
               "sampled_mean_neighbours": sampled_mean, "seconds": round(time.time() - t0, 1)})
-    if sampled_mean != k:
+    # eps is a float32; when no float32 separates a and b the sampled mean
+    # can miss K by a pair or two
+    if abs(sampled_mean - k) > 0.01:
         raise SystemExit("config %d: sampled mean %r != %d" % (cfg, sampled_mean, k))
     return r
 
