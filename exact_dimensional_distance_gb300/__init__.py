@@ -95,10 +95,12 @@ hiss_set_option = _sig("hiss_set_option", ctypes.c_int, [_p, ctypes.c_int, _i64]
 hiss_sort_pairs = _sig("hiss_sort_pairs", ctypes.c_int, [_p, _p, _p, _i64, _i32])
 hiss_exclusive_scan = _sig("hiss_exclusive_scan", ctypes.c_int, [_p, _p, _p, _i64])
 hiss_mask_positions = _sig("hiss_mask_positions", ctypes.c_int, [_p, _p, _i64, _p, ctypes.POINTER(_i64)])
+hiss_exclusive_scan_noalloc = _sig("hiss_exclusive_scan_noalloc", ctypes.c_int, [_p, _p, _p, _i64])
 
 EXPORTED = ["hiss_create", "hiss_destroy", "hiss_build", "hiss_build_host", "hiss_count", "hiss_join",
             "hiss_index", "hiss_last_stats", "hiss_launch_count", "hiss_strerror", "hiss_last_cuda_error",
-            "hiss_set_option", "hiss_sort_pairs", "hiss_exclusive_scan", "hiss_mask_positions"]
+            "hiss_set_option", "hiss_sort_pairs", "hiss_exclusive_scan", "hiss_mask_positions",
+            "hiss_exclusive_scan_noalloc"]
 
 
 class HissError(RuntimeError):

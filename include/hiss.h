@@ -218,6 +218,28 @@ int hiss_exclusive_scan(hiss_ctx *ctx, const int64_t *d_in, int64_t *d_out, int6
  * number to *h_count (host).  d_pos must hold nbits entries. */
 int hiss_mask_positions(hiss_ctx *ctx, const uint32_t *d_words, int64_t nbits, int64_t *d_pos, int64_t *h_count);
 
+/* ---- allocation-free variant ---------------------------------------------
+ * The paper has no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory (a plugin inside a host framework that
+ * owns all device memory through its own pool, or a latency-critical loop that
+ * cannot afford cudaMalloc's implicit device-wide synchronisation).
+ *
+ * Same result as hiss_exclusive_scan (out[i] = sum(in[0..i)), out[n] =
+ * total; in and out may alias), computed by the same kernels on cuda_stream
+ * (a cudaStream_t; NULL = legacy default stream), but with no context and no
+ * allocation: the scratch lives in a static device array of 256 KiB that
+ * every device loading the library holds until the process exits.  The call
+ * is asynchronous with respect to the host.
+ *   - n must be at most 2^26 (67,108,864); larger n returns HISS_E_ARG.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - All calls share the array: calls whose kernels may overlap on the GPU
+ *     (other streams, other host threads) race and must be ordered by the
+ *     caller.  Nothing in the array needs clearing between calls.
+ * Returns HISS_OK, HISS_E_ARG, or HISS_E_CUDA if a launch failed. */
+int hiss_exclusive_scan_noalloc(void *cuda_stream, const int64_t *d_in, int64_t *d_out, int64_t n);
+
 #ifdef __cplusplus
 }
 #endif
