@@ -45,6 +45,25 @@ def load_eps(cfg):
         return json.load(f)[str(cfg)]["eps"]
 
 
+def refine_traffic_per_unit():
+    """DRAM bytes per refinement unit from the committed ncu summary, or None
+    when refine.cu has changed since those counters were taken."""
+    import hashlib
+    src = os.path.join(ROOT, "exact_dimensional_distance_gb300", "csrc", "refine.cu")
+    summ = os.path.join(ROOT, "profiles", "k_refine_gmm_1M_d32.md")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        text = open(summ).read()
+    except OSError:
+        return None
+    if ("sha256 prefix:\n" + sha) not in text and ("sha256 prefix: " + sha) not in text:
+        return None
+    for line in text.splitlines():
+        if line.startswith("traffic_bytes_per_unit:"):
+            return float(line.split(":")[1])
+    return None
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -161,6 +180,8 @@ def run_reference(args, world, rank):
 
 def workload_config(args, eps):
     name, n, d, k = datagen.CONFIGS[args.config]
+    if getattr(args, "n", None):
+        name, n = name + " (reduced instance for profiling)", args.n
     return {"workload": "%s N=%d d=%d mean_neighbours=%d" % (name, n, d, k), "n": n, "d": d, "eps": eps,
             "eps_hex": float(eps).hex(), "batch_bytes": args.batch_bytes, "l2": "flushed between steps",
             "parallelism": "replica per GPU"}
@@ -188,9 +209,11 @@ def main():
     ap.add_argument("--config", type=int, default=2)
     ap.add_argument("--impl", default="hiss", choices=["hiss", "reference"])
     ap.add_argument("--batch-bytes", type=int, default=32 << 30)
-    ap.add_argument("--ref-rows", type=int, default=2000)
+    ap.add_argument("--ref-rows", type=int, default=8000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--n", type=int, default=None,
+                    help="draw a smaller instance of the workload (profiling only; not the benchmark workload)")
     args = ap.parse_args()
     world, rank, local = dist_env()
 
@@ -209,7 +232,7 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
 
-    x = datagen.generate(args.config)
+    x = datagen.generate(args.config, n=args.n)
     eps = load_eps(args.config)
     n, d = x.shape
     stream = torch.cuda.Stream()
@@ -222,7 +245,11 @@ def main():
     def step():
         j.build(xd)
         j.count(eps, out=False)
-        return j.join(eps, args.batch_bytes)
+        st_count = j.stats()
+        st_join = j.join(eps, args.batch_bytes)
+        st_join["ms_index"] = st_count["ms_index"]
+        st_join["ms_build"] = st_count["ms_build"]
+        return st_join
 
     for _ in range(args.warmup):
         st = step()
@@ -253,18 +280,28 @@ def main():
     value = world * pairs * args.steps / t
     clocks = clk.summary()
 
-    # roofline of the refinement kernel: per launch (one per batch), the
-    # algorithmic work is 3 flops per candidate pair and dimension
+    # roofline of the refinement kernel.  Algorithmic work: 3 flops (subtract,
+    # multiply, add) per pair and dimension, over the dimensions each
+    # candidate pair needs with per-pair early termination every 4 dimensions
+    # (counted exactly by hiss_work_profile, outside the timed region).
     st = stats[-1]
     refine_ms = statistics.median(s["ms_refine"] for s in stats)
     refine_launches = st["batches"]
-    flops = 3.0 * cand * d
+    dims_alg, dims_exec = j.work_profile(eps)
+    flops = 3.0 * dims_alg
     pk, pk_kind = peaks()
     peak = fp32_peak_tflops(pk.get("sm_max_mhz", 2070.0))
     achieved = flops / (refine_ms / 1e3) / 1e12
+    tpu = refine_traffic_per_unit()
     roofline = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": None, "kernel": "k_refine", "work": "3 flop x candidate pairs x d (no early exit)",
-                "launches_per_step": refine_launches, "ms_per_launch": refine_ms / refine_launches,
+                "traffic": None if tpu is None else tpu * st["refine_units"] / refine_launches,
+                "traffic_unit": "bytes per launch (ncu DRAM read+write, scaled by units)", "kernel": "k_refine",
+                "work": "3 flop x sum over candidate pairs of the dimensions needed with per-pair exit every 4",
+                "work_per_step_flop": flops, "launches_per_step": refine_launches,
+                "ms_per_launch": refine_ms / refine_launches, "refine_units": st["refine_units"],
+                "executed_frac": 3.0 * dims_exec / (refine_ms / 1e3) / 1e12 / peak,
+                "mean_dims_alg": dims_alg / cand, "mean_dims_executed": dims_exec / cand,
+                "full_dims_frac": 3.0 * cand * d / (refine_ms / 1e3) / 1e12 / peak,
                 "peak_kind": "FP32 lanes x %s sm_max_mhz x 1.5 flop" % pk_kind}
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -95,12 +95,13 @@ hiss_set_option = _sig("hiss_set_option", ctypes.c_int, [_p, ctypes.c_int, _i64]
 hiss_sort_pairs = _sig("hiss_sort_pairs", ctypes.c_int, [_p, _p, _p, _i64, _i32])
 hiss_exclusive_scan = _sig("hiss_exclusive_scan", ctypes.c_int, [_p, _p, _p, _i64])
 hiss_mask_positions = _sig("hiss_mask_positions", ctypes.c_int, [_p, _p, _i64, _p, ctypes.POINTER(_i64)])
+hiss_work_profile = _sig("hiss_work_profile", ctypes.c_int, [_p, _f32, _p])
 hiss_exclusive_scan_noalloc = _sig("hiss_exclusive_scan_noalloc", ctypes.c_int, [_p, _p, _p, _i64])
 
 EXPORTED = ["hiss_create", "hiss_destroy", "hiss_build", "hiss_build_host", "hiss_count", "hiss_join",
             "hiss_index", "hiss_last_stats", "hiss_launch_count", "hiss_strerror", "hiss_last_cuda_error",
             "hiss_set_option", "hiss_sort_pairs", "hiss_exclusive_scan", "hiss_mask_positions",
-            "hiss_exclusive_scan_noalloc"]
+            "hiss_exclusive_scan_noalloc", "hiss_work_profile"]
 
 
 class HissError(RuntimeError):
@@ -262,6 +263,13 @@ class Join:
         s = hiss_stats()
         _check(hiss_last_stats(self._h, ctypes.byref(s)), self._h, "hiss_last_stats")
         return {k: getattr(s, k) for k, _ in hiss_stats._fields_}
+
+    def work_profile(self, eps):
+        """(sum of per-pair early-exit dimensions, dimensions the join's
+        refinement evaluates) over all candidate pairs for eps."""
+        out = (_i64 * 2)()
+        _check(hiss_work_profile(self._h, float(eps), out), self._h, "hiss_work_profile")
+        return int(out[0]), int(out[1])
 
     def launches(self):
         return int(hiss_launch_count(self._h))

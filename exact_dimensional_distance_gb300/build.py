@@ -37,6 +37,11 @@ def _sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
+def _extra_flags():
+    # developer tuning only (e.g. -DHISS_REFINE_MINB=1); empty by default
+    return os.environ.get("HISS_NVCC_EXTRA", "").split()
+
+
 def _stale() -> bool:
     if not os.path.exists(LIB):
         return True
@@ -55,7 +60,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     def compile_one(src):
         obj = os.path.join(OBJ, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc] + ARCH + NVCC_FLAGS + ["-c", src, "-o", obj]
+        cmd = [nvcc] + ARCH + NVCC_FLAGS + _extra_flags() + ["-c", src, "-o", obj]
         if verbose:
             cmd.append("-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)

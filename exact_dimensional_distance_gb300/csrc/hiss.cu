@@ -516,7 +516,9 @@ int do_join(hiss_ctx *ctx, float eps, size_t batch_bytes, const hiss_out *out)
         ra.mask = as<uint32_t>(ctx->mask);
         ra.qcount = as<int32_t>(ctx->qcount);
         ra.d4 = ctx->d4;
+        ra.d = ctx->d;
         ra.eps2 = eps * eps;
+        ra.prof = nullptr;
         CK(cudaEventRecord(ctx->ev[4], s));
         CK(refine(ra, s, &ctx->launches));
         CK(cudaEventRecord(ctx->ev[5], s));
@@ -718,6 +720,41 @@ int hiss_join(hiss_ctx *ctx, float eps, size_t batch_bytes, const hiss_out *out)
     if (!ctx->built) return HISS_E_STATE;
     if (!(eps >= 0.0f) || std::isinf(eps)) return HISS_E_ARG;
     return do_join(ctx, eps, batch_bytes, out);
+}
+
+int hiss_work_profile(hiss_ctx *ctx, float eps, int64_t *out)
+{
+    ST(enter(ctx));
+    if (!out) return HISS_E_ARG;
+    if (!ctx->built) return HISS_E_STATE;
+    if (!(eps >= 0.0f) || std::isinf(eps)) return HISS_E_ARG;
+    ST(ensure_grid(ctx, eps));
+    ST(ensure_tiles(ctx));
+    ST(ensure(ctx, ctx->nb_d, 64));
+    CK(cudaMemsetAsync(ctx->nb_d.p, 0, 16, ctx->stream));
+    RefineArgs ra{};
+    ra.xs = as<float>(ctx->xs);
+    ra.cell_start = as<int32_t>(ctx->cell_start);
+    ra.nbr = as<int32_t>(ctx->nbr);
+    ra.nbr_cnt = as<int32_t>(ctx->nbr_cnt);
+    ra.bound = as<int64_t>(ctx->bound);
+    ra.tile_cell = as<int32_t>(ctx->tile_cell);
+    ra.tile_q0 = as<int32_t>(ctx->tile_q0);
+    ra.tile_nq = as<int32_t>(ctx->tile_nq);
+    ra.tile_word = as<int64_t>(ctx->tile_word);
+    ra.tile_unit = as<int64_t>(ctx->tile_unit);
+    ra.tile_qoff = as<int64_t>(ctx->tile_qoff);
+    ra.t0 = 0;
+    ra.t1 = ctx->T;
+    ra.unit0 = 0;
+    ra.nunits = ctx->total_units;
+    ra.d4 = ctx->d4;
+    ra.d = ctx->d;
+    ra.eps2 = eps * eps;
+    ra.prof = as<int64_t>(ctx->nb_d);
+    CK(refine_profile(ra, ctx->stream, &ctx->launches));
+    CK(cudaMemcpyAsync(out, ctx->nb_d.p, 16, cudaMemcpyDeviceToHost, ctx->stream));
+    return sync(ctx);
 }
 
 int hiss_index(hiss_ctx *ctx, hiss_index_view *v)

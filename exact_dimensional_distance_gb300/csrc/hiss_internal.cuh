@@ -105,11 +105,14 @@ struct RefineArgs {
     uint32_t *mask;             // batch mask
     int32_t *qcount;            // [nq of batch] neighbour count per query (accumulated)
     int d4;
+    int d;                      // true dimension (profile mode caps the last step at d)
     float eps2;
+    int64_t *prof;              // profile mode: [2] counters (sum of per-pair exit dims, executed dims)
 };
 int refine_tq(int d4);
 int refine_chunk(int d4);
 cudaError_t refine(const RefineArgs &a, cudaStream_t s, int64_t *launches);
+cudaError_t refine_profile(const RefineArgs &a, cudaStream_t s, int64_t *launches);
 
 struct CompactArgs {
     const int32_t *ids;         // [n] original id per index row

@@ -38,17 +38,60 @@ struct Tile {
     static constexpr int TQ = 16 * MQ;   // 4 warps x 4 lanes x MQ queries
     static constexpr int TP = 16 * MP;   // 2 warps x 8 lanes x MP candidates
     static constexpr int CH = kChunkTiles * TP;
-    static constexpr int WPW = MP / 4;   // mask words per query per warp column
+    static constexpr int WPW = MP / 4;   // mask words per query row per warp column
 };
 
+// Squared-distance increments of two dimensions (k, k+1) for the thread's
+// MQ x MP block: queries qbase + 4 i, candidates pbase + 8 j.  FIRST starts the
+// sums (the first product is not added to a zeroed register).
+template <int MQ, int MP, bool FIRST>
+__device__ __forceinline__ void block_step2(float (&acc)[MQ][MP], const float *Qs, const float *P, int S, int qbase,
+                                            int pbase, int k)
+{
+    float2 qv[MQ];
+#pragma unroll
+    for (int i = 0; i < MQ; ++i) qv[i] = *reinterpret_cast<const float2 *>(Qs + (qbase + 4 * i) * S + k);
+#pragma unroll
+    for (int j = 0; j < MP; ++j) {
+        const float2 pv = *reinterpret_cast<const float2 *>(P + (pbase + 8 * j) * S + k);
+#pragma unroll
+        for (int i = 0; i < MQ; ++i) {
+            const float e0 = qv[i].x - pv.x, e1 = qv[i].y - pv.y;
+            if (FIRST) acc[i][j] = e0 * e0;
+            else acc[i][j] = fmaf(e0, e0, acc[i][j]);
+            acc[i][j] = fmaf(e1, e1, acc[i][j]);
+        }
+    }
+}
+
 template <int MQ, int MP>
-__global__ void __launch_bounds__(kThreads, 1) k_refine(const RefineArgs a)
+__device__ __forceinline__ float block_min(const float (&acc)[MQ][MP])
+{
+    float m = acc[0][0];
+#pragma unroll
+    for (int i = 0; i < MQ; ++i)
+#pragma unroll
+        for (int j = 0; j < MP; ++j) m = fminf(m, acc[i][j]);
+    return m;
+}
+
+// Resident blocks per SM the register budget is sized for.
+#ifndef HISS_REFINE_MINB
+#define HISS_REFINE_MINB 2
+#endif
+
+// PROF = true: no mask output; instead count, over all candidate pairs, the
+// dimensions a pair needs when it stops at the first multiple of 4 whose
+// partial sum exceeds eps^2 (prof[0]), and the dimensions the warp-level
+// schedule of the PROF = false kernel executes (prof[1]).
+template <int MQ, int MP, bool PROF>
+__global__ void __launch_bounds__(kThreads, HISS_REFINE_MINB) k_refine(const RefineArgs a)
 {
     using T = Tile<MQ, MP>;
     extern __shared__ __align__(16) float smem[];
     __shared__ int32_t s_nstart[kStencil];
     __shared__ int32_t s_vpre[kStencil + 1];
-    __shared__ int64_t s_info[8];
+    __shared__ int64_t s_info[2];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d4 = a.d4, S = tile_stride(d4), C4 = d4 / 4;
@@ -123,11 +166,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_refine(const RefineArgs a)
 
     const int wq = warp >> 1, wp = warp & 1;
     const int lq = lane >> 3, lp = lane & 7;
-    const int qbase = wq * (4 * MQ) + lq;  // query row j: qbase + 4 j
+    const int qbase = wq * (4 * MQ) + lq;  // query row i: qbase + 4 i
     const int pbase = wp * (8 * MP) + lp;  // candidate row j: pbase + 8 j
     const float eps2 = a.eps2;
     uint32_t my_count = 0;                 // neighbours of query row qbase + 4 lp (lp < MQ)
     const int64_t row_word0 = a.tile_word[t] - a.word0;
+    uint64_t prof_alg = 0, prof_exec = 0;
 
     for (int it = 0; it < ntiles; ++it) {
         const int64_t v0 = vbeg + (int64_t)it * T::TP;
@@ -142,35 +186,55 @@ __global__ void __launch_bounds__(kThreads, 1) k_refine(const RefineArgs a)
 
         const float *P = Ps0 + (it & 1) * T::TP * S;
         float acc[MQ][MP];
+        if constexpr (PROF) {
+            // all dimensions, counting live pairs step by step
+            bool warp_live = true;
+            block_step2<MQ, MP, true>(acc, Qs, P, S, qbase, pbase, 0);
+            block_step2<MQ, MP, false>(acc, Qs, P, S, qbase, pbase, 2);
+            int live = 0;
 #pragma unroll
-        for (int i = 0; i < MQ; ++i)
+            for (int i = 0; i < MQ; ++i)
 #pragma unroll
-            for (int j = 0; j < MP; ++j) acc[i][j] = 0.0f;
-
-        for (int k = 0; k < d4; k += 4) {
-            float4 qv[MQ];
-#pragma unroll
-            for (int i = 0; i < MQ; ++i) qv[i] = *reinterpret_cast<const float4 *>(Qs + (qbase + 4 * i) * S + k);
-#pragma unroll
-            for (int j = 0; j < MP; ++j) {
-                const float4 pv = *reinterpret_cast<const float4 *>(P + (pbase + 8 * j) * S + k);
-#pragma unroll
-                for (int i = 0; i < MQ; ++i) {
-                    float e;
-                    e = qv[i].x - pv.x; acc[i][j] = fmaf(e, e, acc[i][j]);
-                    e = qv[i].y - pv.y; acc[i][j] = fmaf(e, e, acc[i][j]);
-                    e = qv[i].z - pv.z; acc[i][j] = fmaf(e, e, acc[i][j]);
-                    e = qv[i].w - pv.w; acc[i][j] = fmaf(e, e, acc[i][j]);
-                }
-            }
-            if (((k + 4) & 7) == 0 && k + 4 < d4) {
-                float m = acc[0][0];
+                for (int j = 0; j < MP; ++j) live += (qbase + 4 * i < nq && v0 + pbase + 8 * j < vend) ? 1 : 0;
+            const int valid = live;
+            prof_alg += (uint64_t)valid * (uint64_t)min(4, a.d);
+            prof_exec += (uint64_t)valid * (uint64_t)min(4, a.d);
+            for (int k = 4; k < d4; k += 4) {
+                live = 0;
 #pragma unroll
                 for (int i = 0; i < MQ; ++i)
 #pragma unroll
-                    for (int j = 0; j < MP; ++j) m = fminf(m, acc[i][j]);
-                if (__all_sync(0xffffffffu, m > eps2)) break;
+                    for (int j = 0; j < MP; ++j) live += (acc[i][j] <= eps2) ? 1 : 0;
+                if (k == 4 || (k & 7) == 0)
+                    if (__all_sync(0xffffffffu, block_min(acc) > eps2)) warp_live = false;
+                if (!__any_sync(0xffffffffu, live > 0) && !warp_live) break;
+                const uint64_t step = (uint64_t)min(4, a.d - k);
+                prof_alg += (uint64_t)live * step;
+                if (warp_live) prof_exec += (uint64_t)valid * step;
+                block_step2<MQ, MP, false>(acc, Qs, P, S, qbase, pbase, k);
+                block_step2<MQ, MP, false>(acc, Qs, P, S, qbase, pbase, k + 2);
             }
+            __syncthreads();
+            continue;
+        }
+        block_step2<MQ, MP, true>(acc, Qs, P, S, qbase, pbase, 0);
+        block_step2<MQ, MP, false>(acc, Qs, P, S, qbase, pbase, 2);
+        // warp-level early termination: checked after 4 and 8 dimensions, then
+        // every 8 (the pairs are in variance order, most leave early)
+        bool any_close = true;
+        for (int k = 4;; k += 4) {
+            if (k == d4) {
+                any_close = __any_sync(0xffffffffu, block_min(acc) <= eps2);
+                break;
+            }
+            if (k == 4 || (k & 7) == 0) {
+                if (__all_sync(0xffffffffu, block_min(acc) > eps2)) {
+                    any_close = false;
+                    break;
+                }
+            }
+            block_step2<MQ, MP, false>(acc, Qs, P, S, qbase, pbase, k);
+            block_step2<MQ, MP, false>(acc, Qs, P, S, qbase, pbase, k + 2);
         }
 
         // one bit per pair; OR across the 8 lanes of a query row; lane lp
@@ -181,12 +245,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_refine(const RefineArgs a)
 #pragma unroll
             for (int wi = 0; wi < T::WPW; ++wi) {
                 uint32_t w = 0;
+                if (any_close) {
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj)
-                    w |= (acc[i][4 * wi + jj] <= eps2 ? 1u : 0u) << (lp + 8 * jj);
-                w |= __shfl_xor_sync(0xffffffffu, w, 1);
-                w |= __shfl_xor_sync(0xffffffffu, w, 2);
-                w |= __shfl_xor_sync(0xffffffffu, w, 4);
+                    for (int jj = 0; jj < 4; ++jj)
+                        w |= (acc[i][4 * wi + jj] <= eps2 ? 1u : 0u) << (lp + 8 * jj);
+                    w |= __shfl_xor_sync(0xffffffffu, w, 1);
+                    w |= __shfl_xor_sync(0xffffffffu, w, 2);
+                    w |= __shfl_xor_sync(0xffffffffu, w, 4);
+                }
                 const int qr = qbase + 4 * i;
                 const int64_t wcol = word_tile + wp * T::WPW + wi;
                 if (lp == i && qr < nq && wcol < W) {
@@ -197,24 +263,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_refine(const RefineArgs a)
         }
         __syncthreads();
     }
+    if constexpr (PROF) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            prof_alg += __shfl_xor_sync(0xffffffffu, prof_alg, o);
+            prof_exec += __shfl_xor_sync(0xffffffffu, prof_exec, o);
+        }
+        if (lane == 0) {
+            atomicAdd(reinterpret_cast<unsigned long long *>(a.prof), (unsigned long long)prof_alg);
+            atomicAdd(reinterpret_cast<unsigned long long *>(a.prof) + 1, (unsigned long long)prof_exec);
+        }
+        return;
+    }
     if (lp < MQ) {
         const int qr = qbase + 4 * lp;
         if (qr < nq && my_count) atomicAdd(&a.qcount[a.tile_qoff[t] - a.q0 + qr], (int32_t)my_count);
     }
 }
 
-template <int MQ, int MP>
+template <int MQ, int MP, bool PROF>
 cudaError_t launch_refine(const RefineArgs &a, cudaStream_t s)
 {
     using T = Tile<MQ, MP>;
     const size_t smem = sizeof(float) * (size_t)(T::TQ + 2 * T::TP) * tile_stride(a.d4);
     static size_t configured = 0;  // largest dynamic shared memory requested so far
     if (smem > configured) {
-        HISS_TRY(cudaFuncSetAttribute(k_refine<MQ, MP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        HISS_TRY(cudaFuncSetAttribute(k_refine<MQ, MP, PROF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)smem));
         configured = smem;
     }
     if (a.nunits <= 0) return cudaSuccess;
-    k_refine<MQ, MP><<<(unsigned)a.nunits, kThreads, smem, s>>>(a);
+    k_refine<MQ, MP, PROF><<<(unsigned)a.nunits, kThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -331,8 +410,15 @@ int refine_tq(int d4) { return d4 <= 128 ? Tile<8, 8>::TQ : Tile<4, 4>::TQ; }
 cudaError_t refine(const RefineArgs &a, cudaStream_t s, int64_t *launches)
 {
     ++*launches;
-    if (a.d4 <= 128) return launch_refine<8, 8>(a, s);
-    return launch_refine<4, 4>(a, s);
+    if (a.d4 <= 128) return launch_refine<8, 8, false>(a, s);
+    return launch_refine<4, 4, false>(a, s);
+}
+
+cudaError_t refine_profile(const RefineArgs &a, cudaStream_t s, int64_t *launches)
+{
+    ++*launches;
+    if (a.d4 <= 128) return launch_refine<8, 8, true>(a, s);
+    return launch_refine<4, 4, true>(a, s);
 }
 
 int refine_chunk(int d4) { return d4 <= 128 ? Tile<8, 8>::CH : Tile<4, 4>::CH; }

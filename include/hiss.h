@@ -198,6 +198,18 @@ const char *hiss_last_cuda_error(const hiss_ctx *ctx);
 enum { HISS_OPT_ALLOC_LIMIT = 1 };
 int hiss_set_option(hiss_ctx *ctx, int option, int64_t value);
 
+/* Work accounting for the refinement roofline (diagnostic; no result
+ * output).  For eps, over every candidate pair of the join: out[0] = the
+ * sum, over pairs, of the dimensions the pair needs when it is abandoned at
+ * the first multiple of 4 dimensions whose variance-ordered float32 partial
+ * sum exceeds eps^2 (capped at d) -- the method's minimal refinement work
+ * with early termination (RT-HiSS Section IV-A); out[1] = the dimensions
+ * hiss_join's refinement kernel actually evaluates, whose warps abandon a
+ * block of pairs only when all of them exceed eps^2 (checked after 4 and 8
+ * dimensions, then every 8).  out is a host int64[2].  Costs about one
+ * join's refinement with no early termination. */
+int hiss_work_profile(hiss_ctx *ctx, float eps, int64_t *out);
+
 /* ---- building blocks exposed for testing ---------------------------------
  * These run the library's own kernels on caller data (device pointers) on
  * the context's stream and return when done. */

@@ -238,3 +238,48 @@ def test_error_statuses():
     assert e.value.status == edd.HISS_E_NOMEM
     rc = edd.hiss_build(None, None, 10, 3)
     assert rc == edd.HISS_E_ARG
+
+
+def _exit_dims_reference(xs, eps, cell_start, nbr, nbr_count, cell_of_row, d):
+    """Sum over candidate pairs of the dimensions needed when a pair stops at
+    the first multiple of 4 whose float32 partial sum exceeds eps^2 (the
+    kernel's own arithmetic: a float32 product, then fused multiply-adds)."""
+    e2 = np.float32(eps) * np.float32(eps)
+    total = 0
+    for q in range(xs.shape[0]):
+        c = cell_of_row[q]
+        cand = np.concatenate([np.arange(cell_start[nb], cell_start[nb + 1]) for nb in nbr[c, :nbr_count[c]]])
+        e = (xs[q][None, :] - xs[cand]).astype(np.float32)
+        acc = (e[:, 0] * e[:, 0]).astype(np.float32)
+        alive = np.ones(cand.size, bool)
+        dims = np.zeros(cand.size, np.int64)
+        for k in range(1, xs.shape[1]):
+            acc = (acc.astype(np.float64) + e[:, k].astype(np.float64) ** 2).astype(np.float32)
+            if (k + 1) % 4 == 0 or k + 1 == xs.shape[1]:
+                step_end = min(k + 1, d)
+                dims[alive] = step_end
+                alive &= acc <= e2
+        total += int(dims.sum())
+    return total
+
+
+def test_work_profile_counts_early_exit_dimensions():
+    edd = _edd()
+    x = datagen.generate(2, n=3000)
+    eps = 6.0
+    j = edd.Join()
+    j.build(torch.from_numpy(x).cuda())
+    j.count(eps)
+    st = j.stats()
+    alg, executed = j.work_profile(eps)
+    ix = j.index()
+    g = oracle.grid(x, eps)
+    perm = oracle.variance_order(oracle.dim_stats(x)[2])
+    d = x.shape[1]
+    xs = x[:, perm][g["order"]]
+    want = _exit_dims_reference(xs, eps, ix["cell_start"].cpu().numpy(),
+                                ix["nbr"].cpu().numpy().reshape(-1, 27), ix["nbr_count"].cpu().numpy(),
+                                ix["cell_of_row"].cpu().numpy(), d)
+    j.close()
+    assert abs(alg - want) <= 1e-6 * want + 8, (alg, want)
+    assert alg <= executed <= st["candidates"] * d
