@@ -3,17 +3,18 @@
 //
 // One thread block refines one unit: a tile of up to TQ queries of one grid
 // cell against one chunk of the cell's stencil candidates (the cells around
-// it, concatenated in stencil order).  The query tile stays in shared memory;
-// candidate tiles of TP points are staged through shared memory with cp.async,
-// double-buffered, gathered row by row from the stencil cells.  Each thread
-// owns an MQ x MP block of (query, candidate) squared distances in registers
-// and adds four dimensions per step (one 16-byte shared load per point), so
-// a step costs 2 * MQ * MP * 4 FP32 instructions against MQ + MP loads.
-// Dimensions are in variance order, so every eight dimensions a warp checks
-// whether all of its partial sums already exceed eps^2 and, if so, skips the
-// rest of the tile (early termination, Section IV-A).  The result is one bit
-// per pair, sum <= eps^2, written to the query's mask row; the popcount of each
-// word is accumulated into the query's neighbour count.
+// it, concatenated in stencil order).  The query tile stays in shared memory
+// (two query rows interleaved per pair row); candidate tiles of TP points are
+// staged through shared memory with cp.async, double-buffered, gathered row by
+// row from the stencil cells.  Each thread owns an MQ x MP block of (query,
+// candidate) squared distances, held as packed float32 pairs, and adds two
+// dimensions per step with f32x2 subtract / multiply-add instructions (one
+// instruction per pair and dimension instead of two).  Dimensions are in
+// variance order, so after 4 and 8 dimensions and then every 8 a warp checks
+// whether all of its partial sums already exceed eps^2 and, if so, leaves the
+// tile (early termination, Section IV-A).  The result is one bit per pair,
+// sum <= eps^2, written to the query's mask row; the popcount of each word is
+// accumulated into the query's neighbour count.
 #include "hiss_internal.cuh"
 
 namespace hiss {
@@ -41,37 +42,101 @@ struct Tile {
     static constexpr int WPW = MP / 4;   // mask words per query row per warp column
 };
 
-// Squared-distance increments of two dimensions (k, k+1) for the thread's
-// MQ x MP block: queries qbase + 4 i, candidates pbase + 8 j.  FIRST starts the
-// sums (the first product is not added to a zeroed register).
-template <int MQ, int MP, bool FIRST>
-__device__ __forceinline__ void block_step2(float (&acc)[MQ][MP], const float *Qs, const float *P, int S, int qbase,
-                                            int pbase, int k)
+// Row stride of the pair-interleaved query tile, in floats: 2 d4 plus padding
+// so that stride / 4 is odd (4 consecutive pair rows hit distinct bank quads).
+__host__ __device__ __forceinline__ int pair_stride(int d4) { return (d4 % 8 == 0) ? 2 * d4 + 4 : 2 * d4 + 8; }
+
+// Packed float32 pairs (two lanes of one 64-bit register), computed with the
+// sm_100-family f32x2 instructions: each is two independent round-to-nearest
+// float32 operations, so the results equal the scalar ones bit for bit.
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 pk(float lo, float hi)
 {
-    float2 qv[MQ];
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float lo_of(f32x2 v)
+{
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    (void)hi;
+    return lo;
+}
+__device__ __forceinline__ float hi_of(f32x2 v)
+{
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    (void)lo;
+    return hi;
+}
+__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b)
+{
+    f32x2 r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b)
+{
+    f32x2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c)
+{
+    f32x2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// The thread's MQ x MP block of squared distances is held as MQ/2 x MP
+// packed pairs: acc[i2][j] = (query i = 2 i2, query i = 2 i2 + 1) x
+// candidate j, i.e. query rows qbase + 8 i2 and qbase + 8 i2 + 4, candidate
+// row pbase + 8 j.  The query tile Q2 stores those two rows interleaved
+// (pair row pid = 16 wq + lq + 4 i2), so one 16-byte load gives both queries'
+// dimensions k and k+1.
+template <int MQ, int MP>
+__device__ __forceinline__ float acc_at(const f32x2 (&acc)[MQ / 2][MP], int i, int j)
+{
+    return (i & 1) ? hi_of(acc[i >> 1][j]) : lo_of(acc[i >> 1][j]);
+}
+
+// Squared-distance increments of dimensions k and k+1 for the whole block.
+// FIRST starts the sums (the first product is not added to a zeroed register).
+template <int MQ, int MP, bool FIRST>
+__device__ __forceinline__ void block_step2(f32x2 (&acc)[MQ / 2][MP], const float *Q2, const float *P, int S2, int S,
+                                            int pidbase, int pbase, int k)
+{
+    f32x2 qa[MQ / 2], qb[MQ / 2];
 #pragma unroll
-    for (int i = 0; i < MQ; ++i) qv[i] = *reinterpret_cast<const float2 *>(Qs + (qbase + 4 * i) * S + k);
+    for (int i2 = 0; i2 < MQ / 2; ++i2) {
+        const float4 v = *reinterpret_cast<const float4 *>(Q2 + (pidbase + 4 * i2) * S2 + 2 * k);
+        qa[i2] = pk(v.x, v.y);  // dimension k of both queries
+        qb[i2] = pk(v.z, v.w);  // dimension k + 1
+    }
 #pragma unroll
     for (int j = 0; j < MP; ++j) {
         const float2 pv = *reinterpret_cast<const float2 *>(P + (pbase + 8 * j) * S + k);
+        const f32x2 p0 = pk(pv.x, pv.x), p1 = pk(pv.y, pv.y);
 #pragma unroll
-        for (int i = 0; i < MQ; ++i) {
-            const float e0 = qv[i].x - pv.x, e1 = qv[i].y - pv.y;
-            if (FIRST) acc[i][j] = e0 * e0;
-            else acc[i][j] = fmaf(e0, e0, acc[i][j]);
-            acc[i][j] = fmaf(e1, e1, acc[i][j]);
+        for (int i2 = 0; i2 < MQ / 2; ++i2) {
+            const f32x2 e0 = sub2(qa[i2], p0), e1 = sub2(qb[i2], p1);
+            if constexpr (FIRST) acc[i2][j] = mul2(e0, e0);
+            else acc[i2][j] = fma2(e0, e0, acc[i2][j]);
+            acc[i2][j] = fma2(e1, e1, acc[i2][j]);
         }
     }
 }
 
 template <int MQ, int MP>
-__device__ __forceinline__ float block_min(const float (&acc)[MQ][MP])
+__device__ __forceinline__ float block_min(const f32x2 (&acc)[MQ / 2][MP])
 {
-    float m = acc[0][0];
+    float m = lo_of(acc[0][0]);
 #pragma unroll
-    for (int i = 0; i < MQ; ++i)
+    for (int i2 = 0; i2 < MQ / 2; ++i2)
 #pragma unroll
-        for (int j = 0; j < MP; ++j) m = fminf(m, acc[i][j]);
+        for (int j = 0; j < MP; ++j) m = fminf(m, fminf(lo_of(acc[i2][j]), hi_of(acc[i2][j])));
     return m;
 }
 
@@ -94,9 +159,9 @@ __global__ void __launch_bounds__(kThreads, HISS_REFINE_MINB) k_refine(const Ref
     __shared__ int64_t s_info[2];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int d4 = a.d4, S = tile_stride(d4), C4 = d4 / 4;
-    float *Qs = smem;
-    float *Ps0 = smem + T::TQ * S;
+    const int d4 = a.d4, S = tile_stride(d4), S2 = pair_stride(d4), C4 = d4 / 4;
+    float *Q2 = smem;
+    float *Ps0 = smem + (T::TQ / 2) * S2;
 
     if (tid == 0) {
         const int64_t u = a.unit0 + blockIdx.x;
@@ -128,12 +193,17 @@ __global__ void __launch_bounds__(kThreads, HISS_REFINE_MINB) k_refine(const Ref
         for (int i = 1; i <= ns; ++i) s_vpre[i] += s_vpre[i - 1];
     }
 
-    // query tile: rows q0 .. q0+nq, +inf beyond
-    for (int idx = tid; idx < T::TQ * C4; idx += kThreads) {
-        const int r = idx / C4, cc = idx - r * C4;
-        float *dst = Qs + r * S + 4 * cc;
-        if (r < nq) cp_async16(dst, a.xs + (int64_t)(q0 + r) * d4 + 4 * cc);
-        else *reinterpret_cast<float4 *>(dst) = make_float4(INFINITY, INFINITY, INFINITY, INFINITY);
+    // query tile, pair-interleaved: pair row pid holds rows a = 8 (pid / 4) +
+    // pid % 4 and a + 4, dimension by dimension; rows >= nq are +inf
+    for (int idx = tid; idx < (T::TQ / 2) * C4; idx += kThreads) {
+        const int pid = idx / C4, cc = idx - pid * C4;
+        const int ra = 8 * (pid >> 2) + (pid & 3), rb = ra + 4;
+        const float4 inf4 = make_float4(INFINITY, INFINITY, INFINITY, INFINITY);
+        const float4 x = ra < nq ? *reinterpret_cast<const float4 *>(a.xs + (int64_t)(q0 + ra) * d4 + 4 * cc) : inf4;
+        const float4 y = rb < nq ? *reinterpret_cast<const float4 *>(a.xs + (int64_t)(q0 + rb) * d4 + 4 * cc) : inf4;
+        float4 *dst = reinterpret_cast<float4 *>(Q2 + pid * S2 + 8 * cc);
+        dst[0] = make_float4(x.x, y.x, x.y, y.y);
+        dst[1] = make_float4(x.z, y.z, x.w, y.w);
     }
     __syncthreads();  // s_vpre complete
 
@@ -167,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, HISS_REFINE_MINB) k_refine(const Ref
     const int wq = warp >> 1, wp = warp & 1;
     const int lq = lane >> 3, lp = lane & 7;
     const int qbase = wq * (4 * MQ) + lq;  // query row i: qbase + 4 i
+    const int pidbase = wq * (2 * MQ) + lq; // pair row of queries 2 i2, 2 i2 + 1: pidbase + 4 i2
     const int pbase = wp * (8 * MP) + lp;  // candidate row j: pbase + 8 j
     const float eps2 = a.eps2;
     uint32_t my_count = 0;                 // neighbours of query row qbase + 4 lp (lp < MQ)
@@ -185,12 +256,12 @@ __global__ void __launch_bounds__(kThreads, HISS_REFINE_MINB) k_refine(const Ref
         __syncthreads();
 
         const float *P = Ps0 + (it & 1) * T::TP * S;
-        float acc[MQ][MP];
+        f32x2 acc[MQ / 2][MP];
         if constexpr (PROF) {
             // all dimensions, counting live pairs step by step
             bool warp_live = true;
-            block_step2<MQ, MP, true>(acc, Qs, P, S, qbase, pbase, 0);
-            block_step2<MQ, MP, false>(acc, Qs, P, S, qbase, pbase, 2);
+            block_step2<MQ, MP, true>(acc, Q2, P, S2, S, pidbase, pbase, 0);
+            block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, 2);
             int live = 0;
 #pragma unroll
             for (int i = 0; i < MQ; ++i)
@@ -204,37 +275,37 @@ __global__ void __launch_bounds__(kThreads, HISS_REFINE_MINB) k_refine(const Ref
 #pragma unroll
                 for (int i = 0; i < MQ; ++i)
 #pragma unroll
-                    for (int j = 0; j < MP; ++j) live += (acc[i][j] <= eps2) ? 1 : 0;
+                    for (int j = 0; j < MP; ++j) live += (acc_at<MQ, MP>(acc, i, j) <= eps2) ? 1 : 0;
                 if (k == 4 || (k & 7) == 0)
-                    if (__all_sync(0xffffffffu, block_min(acc) > eps2)) warp_live = false;
+                    if (__all_sync(0xffffffffu, block_min<MQ, MP>(acc) > eps2)) warp_live = false;
                 if (!__any_sync(0xffffffffu, live > 0) && !warp_live) break;
                 const uint64_t step = (uint64_t)min(4, a.d - k);
                 prof_alg += (uint64_t)live * step;
                 if (warp_live) prof_exec += (uint64_t)valid * step;
-                block_step2<MQ, MP, false>(acc, Qs, P, S, qbase, pbase, k);
-                block_step2<MQ, MP, false>(acc, Qs, P, S, qbase, pbase, k + 2);
+                block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k);
+                block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k + 2);
             }
             __syncthreads();
             continue;
         }
-        block_step2<MQ, MP, true>(acc, Qs, P, S, qbase, pbase, 0);
-        block_step2<MQ, MP, false>(acc, Qs, P, S, qbase, pbase, 2);
+        block_step2<MQ, MP, true>(acc, Q2, P, S2, S, pidbase, pbase, 0);
+        block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, 2);
         // warp-level early termination: checked after 4 and 8 dimensions, then
         // every 8 (the pairs are in variance order, most leave early)
         bool any_close = true;
         for (int k = 4;; k += 4) {
             if (k == d4) {
-                any_close = __any_sync(0xffffffffu, block_min(acc) <= eps2);
+                any_close = __any_sync(0xffffffffu, block_min<MQ, MP>(acc) <= eps2);
                 break;
             }
             if (k == 4 || (k & 7) == 0) {
-                if (__all_sync(0xffffffffu, block_min(acc) > eps2)) {
+                if (__all_sync(0xffffffffu, block_min<MQ, MP>(acc) > eps2)) {
                     any_close = false;
                     break;
                 }
             }
-            block_step2<MQ, MP, false>(acc, Qs, P, S, qbase, pbase, k);
-            block_step2<MQ, MP, false>(acc, Qs, P, S, qbase, pbase, k + 2);
+            block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k);
+            block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k + 2);
         }
 
         // one bit per pair; OR across the 8 lanes of a query row; lane lp
@@ -248,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, HISS_REFINE_MINB) k_refine(const Ref
                 if (any_close) {
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj)
-                        w |= (acc[i][4 * wi + jj] <= eps2 ? 1u : 0u) << (lp + 8 * jj);
+                        w |= (acc_at<MQ, MP>(acc, i, 4 * wi + jj) <= eps2 ? 1u : 0u) << (lp + 8 * jj);
                     w |= __shfl_xor_sync(0xffffffffu, w, 1);
                     w |= __shfl_xor_sync(0xffffffffu, w, 2);
                     w |= __shfl_xor_sync(0xffffffffu, w, 4);
@@ -285,7 +356,7 @@ template <int MQ, int MP, bool PROF>
 cudaError_t launch_refine(const RefineArgs &a, cudaStream_t s)
 {
     using T = Tile<MQ, MP>;
-    const size_t smem = sizeof(float) * (size_t)(T::TQ + 2 * T::TP) * tile_stride(a.d4);
+    const size_t smem = sizeof(float) * ((size_t)(T::TQ / 2) * pair_stride(a.d4) + (size_t)2 * T::TP * tile_stride(a.d4));
     static size_t configured = 0;  // largest dynamic shared memory requested so far
     if (smem > configured) {
         HISS_TRY(cudaFuncSetAttribute(k_refine<MQ, MP, PROF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
