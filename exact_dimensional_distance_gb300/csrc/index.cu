@@ -69,26 +69,44 @@ __global__ void __launch_bounds__(kT) k_stats_partial(const float *__restrict__ 
     }
 }
 
-__global__ void k_stats_final(const float *x, int64_t n, int d, const double *partial, int64_t nblocks,
-                              double *out)
+// One block per dimension: the block partials are reduced in a fixed order
+// (strided sums, then a tree), so the result does not depend on timing.
+__global__ void __launch_bounds__(kT) k_stats_final(const float *x, int64_t n, int d, const double *partial,
+                                                    int64_t nblocks, double *out)
 {
-    const int k = blockIdx.x * blockDim.x + threadIdx.x;
-    if (k >= d) return;
+    __shared__ double s_a[kT], s_b[kT], s_lo[kT], s_hi[kT];
+    const int k = blockIdx.x;
     double a = 0.0, b = 0.0, lo = INFINITY, hi = -INFINITY;
-    for (int64_t i = 0; i < nblocks; ++i) {
+    for (int64_t i = threadIdx.x; i < nblocks; i += kT) {
         const double *p = partial + ((size_t)i * d + k) * 4;
         a += p[0];
         b += p[1];
         lo = fmin(lo, p[2]);
         hi = fmax(hi, p[3]);
     }
-    const double mean_shift = a / (double)n;
-    double var = b / (double)n - mean_shift * mean_shift;
-    if (var < 0.0) var = 0.0;
-    out[0 * d + k] = lo;
-    out[1 * d + k] = hi;
-    out[2 * d + k] = (double)x[k] + mean_shift;
-    out[3 * d + k] = var;
+    s_a[threadIdx.x] = a;
+    s_b[threadIdx.x] = b;
+    s_lo[threadIdx.x] = lo;
+    s_hi[threadIdx.x] = hi;
+    __syncthreads();
+    for (int o = kT / 2; o > 0; o >>= 1) {
+        if (threadIdx.x < o) {
+            s_a[threadIdx.x] += s_a[threadIdx.x + o];
+            s_b[threadIdx.x] += s_b[threadIdx.x + o];
+            s_lo[threadIdx.x] = fmin(s_lo[threadIdx.x], s_lo[threadIdx.x + o]);
+            s_hi[threadIdx.x] = fmax(s_hi[threadIdx.x], s_hi[threadIdx.x + o]);
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        const double mean_shift = s_a[0] / (double)n;
+        double var = s_b[0] / (double)n - mean_shift * mean_shift;
+        if (var < 0.0) var = 0.0;
+        out[0 * d + k] = s_lo[0];
+        out[1 * d + k] = s_hi[0];
+        out[2 * d + k] = (double)x[k] + mean_shift;
+        out[3 * d + k] = var;
+    }
 }
 
 __global__ void k_permute_pad(const float *__restrict__ x, int64_t n, int d, int d4, const int32_t *__restrict__ perm,
@@ -245,7 +263,7 @@ __global__ void k_tile_fill(const uint32_t *__restrict__ order, const int32_t *_
     const uint32_t c = order[i];
     const int32_t s0 = cell_start[c], sz = cell_start[c + 1] - s0;
     const int64_t B = bound[c];
-    const int64_t words = (B + 31) / 32;
+    const int64_t words = (((B + 31) / 32) + 3) & ~int64_t(3);  // mask row stride: 16-byte rows
     const int64_t units = (B + chunk - 1) / chunk;
     int64_t t = tile_off[i];
     for (int32_t q = 0; q < sz; q += tq, ++t) {
@@ -308,7 +326,7 @@ cudaError_t dim_stats(const float *x, int64_t n, int d, double *partial, double 
     const int64_t rows = (n + nb - 1) / nb;
     HISS_TRY(cudaMemsetAsync(nonfinite, 0, sizeof(int), s));
     k_stats_partial<<<(unsigned)nb, kT, 0, s>>>(x, n, d, rows, partial, nonfinite);
-    k_stats_final<<<blocks_for(d, 64), 64, 0, s>>>(x, n, d, partial, nb, out);
+    k_stats_final<<<d, kT, 0, s>>>(x, n, d, partial, nb, out);
     *launches += 2;
     return cudaGetLastError();
 }

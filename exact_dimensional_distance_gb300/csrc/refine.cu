@@ -129,6 +129,14 @@ __device__ __forceinline__ void block_step2(f32x2 (&acc)[MQ / 2][MP], const floa
     }
 }
 
+__device__ __forceinline__ float min3(float a, float b, float c)
+{
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Smallest of the thread's MQ x MP partial sums (three-input minima).
 template <int MQ, int MP>
 __device__ __forceinline__ float block_min(const f32x2 (&acc)[MQ / 2][MP])
 {
@@ -136,7 +144,7 @@ __device__ __forceinline__ float block_min(const f32x2 (&acc)[MQ / 2][MP])
 #pragma unroll
     for (int i2 = 0; i2 < MQ / 2; ++i2)
 #pragma unroll
-        for (int j = 0; j < MP; ++j) m = fminf(m, fminf(lo_of(acc[i2][j]), hi_of(acc[i2][j])));
+        for (int j = 0; j < MP; ++j) m = min3(m, lo_of(acc[i2][j]), hi_of(acc[i2][j]));
     return m;
 }
 
@@ -157,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, HISS_REFINE_MINB) k_refine(const Ref
     __shared__ int32_t s_nstart[kStencil];
     __shared__ int32_t s_vpre[kStencil + 1];
     __shared__ int64_t s_info[2];
+    __shared__ int32_t s_src[2][T::TP];  // source row of each candidate row of a staged tile (-1: none)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d4 = a.d4, S = tile_stride(d4), S2 = pair_stride(d4), C4 = d4 / 4;
@@ -180,7 +189,8 @@ __global__ void __launch_bounds__(kThreads, HISS_REFINE_MINB) k_refine(const Ref
     const int32_t q0 = a.tile_q0[t];
     const int nq = a.tile_nq[t];
     const int64_t B = a.bound[c];
-    const int64_t W = (B + 31) >> 5;
+    const int64_t W = (B + 31) >> 5;           // meaningful words of a mask row
+    const int64_t W4 = (W + 3) & ~int64_t(3);  // row stride (16-byte rows)
     const int ns = a.nbr_cnt[c];
     if (tid < ns) {
         const int32_t nb = a.nbr[(int64_t)c * kStencil + tid];
@@ -211,27 +221,46 @@ __global__ void __launch_bounds__(kThreads, HISS_REFINE_MINB) k_refine(const Ref
     const int64_t vend = min(B, vbeg + (int64_t)T::CH);
     const int ntiles = (int)((vend - vbeg + T::TP - 1) / T::TP);
 
-    auto load_p = [&](int buf, int64_t v0) {
-        float *P = Ps0 + buf * T::TP * S;
-        for (int idx = tid; idx < T::TP * C4; idx += kThreads) {
-            const int r = idx / C4, cc = idx - r * C4;
-            float *dst = P + r * S + 4 * cc;
+    // source rows of candidate tile v0 .. v0 + TP, looked up once per row
+    auto fill_src = [&](int buf, int64_t v0) {
+        for (int r = tid; r < T::TP; r += kThreads) {
             const int64_t v = v0 + r;
+            int32_t src = -1;
             if (v < vend) {
                 int lo = 0, hi = ns - 1;  // last slot with s_vpre[slot] <= v
                 while (lo < hi) {
                     const int mid = (lo + hi + 1) >> 1;
                     if (s_vpre[mid] <= v) lo = mid; else hi = mid - 1;
                 }
-                const int64_t src = s_nstart[lo] + (v - s_vpre[lo]);
-                cp_async16(dst, a.xs + src * d4 + 4 * cc);
-            } else {
-                *reinterpret_cast<float4 *>(dst) = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                src = s_nstart[lo] + (int32_t)(v - s_vpre[lo]);
+            }
+            s_src[buf][r] = src;
+        }
+    };
+    // this thread's first (row, 16-byte chunk) of a staged tile and the step
+    const int r_first = tid / C4, c_first = tid - (tid / C4) * C4;
+    const int r_step = kThreads / C4, c_step = kThreads - (kThreads / C4) * C4;
+    auto load_p = [&](int buf) {
+        float *P = Ps0 + buf * T::TP * S;
+        int r = r_first, cc = c_first;
+        for (int idx = tid; idx < T::TP * C4; idx += kThreads) {
+            float *dst = P + r * S + 4 * cc;
+            const int32_t src = s_src[buf][r];
+            if (src >= 0) cp_async16(dst, a.xs + (int64_t)src * d4 + 4 * cc);
+            else *reinterpret_cast<float4 *>(dst) = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            r += r_step;
+            cc += c_step;
+            if (cc >= C4) {
+                cc -= C4;
+                ++r;
             }
         }
     };
 
-    load_p(0, vbeg);
+    fill_src(0, vbeg);
+    if (ntiles > 1) fill_src(1, vbeg + T::TP);
+    __syncthreads();
+    load_p(0);
     cp_async_commit();
 
     const int wq = warp >> 1, wp = warp & 1;
@@ -247,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, HISS_REFINE_MINB) k_refine(const Ref
     for (int it = 0; it < ntiles; ++it) {
         const int64_t v0 = vbeg + (int64_t)it * T::TP;
         if (it + 1 < ntiles) {
-            load_p((it + 1) & 1, v0 + T::TP);
+            load_p((it + 1) & 1);
             cp_async_commit();
             cp_async_wait<1>();
         } else {
@@ -285,6 +314,7 @@ __global__ void __launch_bounds__(kThreads, HISS_REFINE_MINB) k_refine(const Ref
                 block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k);
                 block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k + 2);
             }
+            if (it + 2 < ntiles) fill_src(it & 1, v0 + 2 * T::TP);
             __syncthreads();
             continue;
         }
@@ -311,27 +341,36 @@ __global__ void __launch_bounds__(kThreads, HISS_REFINE_MINB) k_refine(const Ref
         // one bit per pair; OR across the 8 lanes of a query row; lane lp
         // writes the words of query j = lp
         const int64_t word_tile = v0 >> 5;
+        if (any_close) {
 #pragma unroll
-        for (int i = 0; i < MQ; ++i) {
+            for (int i = 0; i < MQ; ++i) {
 #pragma unroll
-            for (int wi = 0; wi < T::WPW; ++wi) {
-                uint32_t w = 0;
-                if (any_close) {
+                for (int wi = 0; wi < T::WPW; ++wi) {
+                    uint32_t w = 0;
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj)
                         w |= (acc_at<MQ, MP>(acc, i, 4 * wi + jj) <= eps2 ? 1u : 0u) << (lp + 8 * jj);
                     w |= __shfl_xor_sync(0xffffffffu, w, 1);
                     w |= __shfl_xor_sync(0xffffffffu, w, 2);
                     w |= __shfl_xor_sync(0xffffffffu, w, 4);
-                }
-                const int qr = qbase + 4 * i;
-                const int64_t wcol = word_tile + wp * T::WPW + wi;
-                if (lp == i && qr < nq && wcol < W) {
-                    a.mask[row_word0 + (int64_t)qr * W + wcol] = w;
-                    my_count += __popc(w);
+                    const int qr = qbase + 4 * i;
+                    const int64_t wcol = word_tile + wp * T::WPW + wi;
+                    if (lp == i && qr < nq && wcol < W) {
+                        a.mask[row_word0 + (int64_t)qr * W4 + wcol] = w;
+                        my_count += __popc(w);
+                    }
                 }
             }
+        } else if (lp < MQ && qbase + 4 * lp < nq) {
+            // no pair of the warp is within eps: zero words for this lane's row
+            uint32_t *row = a.mask + row_word0 + (int64_t)(qbase + 4 * lp) * W4;
+#pragma unroll
+            for (int wi = 0; wi < T::WPW; ++wi) {
+                const int64_t wcol = word_tile + wp * T::WPW + wi;
+                if (wcol < W) row[wcol] = 0u;
+            }
         }
+        if (it + 2 < ntiles) fill_src(it & 1, v0 + 2 * T::TP);
         __syncthreads();
     }
     if constexpr (PROF) {
@@ -390,14 +429,15 @@ __global__ void __launch_bounds__(kCompactWarps * 32) k_compact(const CompactArg
     const int32_t row = a.tile_q0[t] + (int32_t)i;
     const int64_t B = a.bound[c];
     const int64_t W = (B + 31) >> 5;
-    const int64_t woff = a.tile_word[t] - a.word0 + i * W;
+    const int64_t W4 = (W + 3) & ~int64_t(3);
+    const int64_t woff = a.tile_word[t] - a.word0 + i * W4;
     if (lane == 0) {
         a.query_ids[gq] = a.ids[row];
         a.query_rows[gq] = row;
         if (a.cand) a.cand[gq] = B;
         if (a.mask_row_ptr) {
             a.mask_row_ptr[gq] = woff;
-            if (gq == a.nq - 1) a.mask_row_ptr[a.nq] = woff + W;
+            if (gq == a.nq - 1) a.mask_row_ptr[a.nq] = woff + W4;
         }
     }
     if (!a.cols) return;
@@ -417,13 +457,21 @@ __global__ void __launch_bounds__(kCompactWarps * 32) k_compact(const CompactArg
     if (lane < ns) s_vpre[warp][lane] = incl - sz;
     __syncwarp();
 
-    const uint32_t *mrow = a.mask + woff;
+    // rows are 16-byte aligned: each lane takes four words per step
+    const uint4 *mrow = reinterpret_cast<const uint4 *>(a.mask + woff);
     int32_t *out = a.cols + a.row_ptr[gq];
     int64_t run = 0;
-    for (int64_t w0 = 0; w0 < W; w0 += 32) {
-        const int64_t w = w0 + lane;
-        uint32_t word = w < W ? mrow[w] : 0u;
-        const int cnt = __popc(word);
+    for (int64_t w0 = 0; w0 < W; w0 += 128) {
+        const int64_t w = w0 + 4 * lane;
+        uint32_t wd[4] = {0u, 0u, 0u, 0u};
+        if (w < W) {
+            const uint4 v = mrow[w >> 2];
+            wd[0] = v.x;
+            wd[1] = w + 1 < W ? v.y : 0u;
+            wd[2] = w + 2 < W ? v.z : 0u;
+            wd[3] = w + 3 < W ? v.w : 0u;
+        }
+        const int cnt = __popc(wd[0]) + __popc(wd[1]) + __popc(wd[2]) + __popc(wd[3]);
         int ex = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -432,16 +480,20 @@ __global__ void __launch_bounds__(kCompactWarps * 32) k_compact(const CompactArg
         }
         const int total = __shfl_sync(0xffffffffu, ex, 31);
         int64_t pos = run + ex - cnt;
-        while (word) {
-            const int b = __ffs(word) - 1;
-            word &= word - 1;
-            const int64_t v = w * 32 + b;
-            int l = 0, h = ns - 1;
-            while (l < h) {
-                const int m = (l + h + 1) >> 1;
-                if (s_vpre[warp][m] <= v) l = m; else h = m - 1;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            uint32_t word = wd[h];
+            while (word) {
+                const int b = __ffs(word) - 1;
+                word &= word - 1;
+                const int64_t v = (w + h) * 32 + b;
+                int l = 0, hh = ns - 1;
+                while (l < hh) {
+                    const int m = (l + hh + 1) >> 1;
+                    if (s_vpre[warp][m] <= v) l = m; else hh = m - 1;
+                }
+                out[pos++] = a.ids[s_start[warp][l] + (v - s_vpre[warp][l])];
             }
-            out[pos++] = a.ids[s_start[warp][l] + (v - s_vpre[warp][l])];
         }
         run += total;
     }

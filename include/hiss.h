@@ -101,7 +101,9 @@ typedef struct {
     int64_t index;              /* batch number, 0-based */
     int64_t nq;                 /* queries in this batch */
     const int64_t *query_ids;   /* [nq] original id of each query, in processing order */
-    const int64_t *row_ptr;     /* [nq+1] CSR: offsets into cols; MASK: offsets into mask (32-bit words) */
+    const int64_t *row_ptr;     /* [nq+1] CSR: offsets into cols; MASK: offsets into mask (32-bit words;
+                                   rows are padded to a multiple of 4 words, bits at or beyond cand[i] are 0
+                                   or unspecified) */
     const int32_t *cols;        /* CSR: [nnz] original ids of the neighbours (unordered within a row); else NULL */
     const uint32_t *mask;       /* MASK: [n_words] result mask; else NULL */
     const int64_t *cand;        /* MASK: [nq] candidate count B_q (bits used in the row); else NULL */
@@ -131,7 +133,8 @@ typedef struct {
  * orders the grid cells by decreasing work |cell| * B_cell so that the
  * largest work goes first (RT-HiSS Section IV-D), and cuts them, one query
  * tile at a time, into batches whose result mask (one bit per candidate
- * pair, ceil(B_q / 32) words per query) fits in batch_bytes.  Each batch is
+ * pair, ceil(B_q / 32) words per query rounded up to a multiple of 4) fits
+ * in batch_bytes.  Each batch is
  * refined exactly on CUDA cores (float32 squared distances summed in
  * variance order, pair rejected once the partial sum exceeds eps^2; bit =
  * sum <= eps^2), compacted from the mask to CSR (Section IV-F1) unless
