@@ -10,7 +10,7 @@
 // candidate) squared distances, held as packed float32 pairs, and adds two
 // dimensions per step with f32x2 subtract / multiply-add instructions (one
 // instruction per pair and dimension instead of two).  Dimensions are in
-// variance order, so after 4 and 8 dimensions and then every 8 a warp checks
+// variance order, so after 4, 8 and 12 dimensions and then every 8 a warp checks
 // whether all of its partial sums already exceed eps^2 and, if so, leaves the
 // tile (early termination, Section IV-A).  The result is one bit per pair,
 // sum <= eps^2, written to the query's mask row; the popcount of each word is
@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, HISS_REFINE_MINB) k_refine(const Ref
                 for (int i = 0; i < MQ; ++i)
 #pragma unroll
                     for (int j = 0; j < MP; ++j) live += (acc_at<MQ, MP>(acc, i, j) <= eps2) ? 1 : 0;
-                if (k == 4 || (k & 7) == 0)
+                if (k < 16 || (k & 7) == 0)
                     if (__all_sync(0xffffffffu, block_min<MQ, MP>(acc) > eps2)) warp_live = false;
                 if (!__any_sync(0xffffffffu, live > 0) && !warp_live) break;
                 const uint64_t step = (uint64_t)min(4, a.d - k);
@@ -320,15 +320,15 @@ __global__ void __launch_bounds__(kThreads, HISS_REFINE_MINB) k_refine(const Ref
         }
         block_step2<MQ, MP, true>(acc, Q2, P, S2, S, pidbase, pbase, 0);
         block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, 2);
-        // warp-level early termination: checked after 4 and 8 dimensions, then
-        // every 8 (the pairs are in variance order, most leave early)
+        // warp-level early termination: checked after 4, 8 and 12 dimensions,
+        // then every 8 (the pairs are in variance order, most leave early)
         bool any_close = true;
         for (int k = 4;; k += 4) {
             if (k == d4) {
                 any_close = __any_sync(0xffffffffu, block_min<MQ, MP>(acc) <= eps2);
                 break;
             }
-            if (k == 4 || (k & 7) == 0) {
+            if (k < 16 || (k & 7) == 0) {
                 if (__all_sync(0xffffffffu, block_min<MQ, MP>(acc) > eps2)) {
                     any_close = false;
                     break;
