@@ -136,6 +136,20 @@ class Clocks:
         return out
 
 
+def aggregate(t_local, units_local, dist=None, device=None):
+    """Whole-job timing across ranks: the slowest rank's time and the units
+    (result pairs) all ranks processed.  Works on any torch.distributed
+    backend (nccl on the GPUs, gloo in the CPU tests)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(t_local), int(units_local)
+    import torch
+    t = torch.tensor([float(t_local)], dtype=torch.float64, device=device)
+    u = torch.tensor([int(units_local)], dtype=torch.int64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(u.item())
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -270,14 +284,10 @@ def main():
     launches = j.launches() - launches0
     ms = [a.elapsed_time(b) for a, b in ev]
     t_local = sum(ms) / 1e3
-    t = t_local
-    if dist:
-        tt = torch.tensor([t_local], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t = float(tt.item())
     pairs = stats[-1]["pairs"]
     cand = stats[-1]["candidates"]
-    value = world * pairs * args.steps / t
+    t, units = aggregate(t_local, pairs * args.steps, dist, torch.device("cuda", local))
+    value = units / t
     clocks = clk.summary()
 
     # roofline of the refinement kernel.  Algorithmic work: 3 flops (subtract,
@@ -309,6 +319,7 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": workload_config(args, eps), "gpu_launches": int(launches),
             "candidate_evals_per_s": world * cand * args.steps / t,
+            "replicas": world,
             "pairs_per_step": pairs, "candidates_per_step": cand,
             "pruning": 1.0 - cand / float(n) ** 2,
             "phase_ms": {k: st[k] for k in ("ms_build", "ms_index", "ms_count", "ms_refine", "ms_compact",
@@ -332,12 +343,14 @@ def main():
         e2e_step()
         torch.cuda.synchronize()
         d2h[0] = 0
+        if dist:
+            dist.barrier()
         t0 = time.perf_counter()
         for _ in range(args.steps):
             e2e_step()
         torch.cuda.synchronize()
-        te = time.perf_counter() - t0
-        line["e2e"] = {"value": world * pairs * args.steps / te, "unit": UNIT,
+        te, e2e_units = aggregate(time.perf_counter() - t0, pairs * args.steps, dist, torch.device("cuda", local))
+        line["e2e"] = {"value": e2e_units / te, "unit": UNIT,
                        "h2d_bytes_per_step": int(x.nbytes), "d2h_bytes_per_step": int(d2h[0] // args.steps),
                        "ms_per_step": 1e3 * te / args.steps}
 
