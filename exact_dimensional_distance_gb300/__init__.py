@@ -96,12 +96,15 @@ hiss_sort_pairs = _sig("hiss_sort_pairs", ctypes.c_int, [_p, _p, _p, _i64, _i32]
 hiss_exclusive_scan = _sig("hiss_exclusive_scan", ctypes.c_int, [_p, _p, _p, _i64])
 hiss_mask_positions = _sig("hiss_mask_positions", ctypes.c_int, [_p, _p, _i64, _p, ctypes.POINTER(_i64)])
 hiss_work_profile = _sig("hiss_work_profile", ctypes.c_int, [_p, _f32, _p])
+hiss_join_queries = _sig("hiss_join_queries", ctypes.c_int,
+                         [_p, _p, _i64, _f32, ctypes.c_size_t, ctypes.POINTER(hiss_out)])
+hiss_count_queries = _sig("hiss_count_queries", ctypes.c_int, [_p, _p, _i64, _f32, _p])
 hiss_exclusive_scan_noalloc = _sig("hiss_exclusive_scan_noalloc", ctypes.c_int, [_p, _p, _p, _i64])
 
 EXPORTED = ["hiss_create", "hiss_destroy", "hiss_build", "hiss_build_host", "hiss_count", "hiss_join",
             "hiss_index", "hiss_last_stats", "hiss_launch_count", "hiss_strerror", "hiss_last_cuda_error",
             "hiss_set_option", "hiss_sort_pairs", "hiss_exclusive_scan", "hiss_mask_positions",
-            "hiss_exclusive_scan_noalloc", "hiss_work_profile"]
+            "hiss_exclusive_scan_noalloc", "hiss_work_profile", "hiss_join_queries", "hiss_count_queries"]
 
 
 class HissError(RuntimeError):
@@ -214,6 +217,59 @@ class Join:
             raise err[0]
         _check(rc, self._h, "hiss_join")
         return self.stats()
+
+    def _run(self, call, on_batch):
+        err = []
+
+        def cb(user, bptr):
+            try:
+                on_batch(bptr.contents)
+                return 0
+            except BaseException as e:  # surfaced after the call returns
+                err.append(e)
+                return 1
+
+        fn = HISS_BATCH_FN(cb) if on_batch is not None else HISS_BATCH_FN()
+        rc = call(fn)
+        if err:
+            raise err[0]
+        return rc
+
+    def join_queries(self, queries, eps, batch_bytes=0, mode=HISS_OUT_CSR, copy_to_host=False, on_batch=None):
+        """Semi-join of the query points (torch CUDA float32 (nq, d)) against
+        the built dataset; on_batch as in ``join``.  Returns the stats dict."""
+        q = queries.contiguous()
+        assert q.is_cuda and q.dim() == 2 and q.shape[1] == self.d
+
+        def call(fn):
+            out = hiss_out(mode, 1 if copy_to_host else 0, fn, None)
+            return hiss_join_queries(self._h, q.data_ptr() if q.numel() else None, q.shape[0], float(eps),
+                                     int(batch_bytes), ctypes.byref(out))
+
+        _check(self._run(call, on_batch), self._h, "hiss_join_queries")
+        return self.stats()
+
+    def join_queries_sets(self, queries, eps, batch_bytes=0):
+        """Semi-join result as {query row: numpy array of data ids}."""
+        res = {}
+
+        def take(b):
+            q = _host_array(b.query_ids, b.nq, np.int64)
+            rp = _host_array(b.row_ptr, b.nq + 1, np.int64)
+            cols = _host_array(b.cols, b.nnz, np.int32)
+            for i in range(b.nq):
+                res[int(q[i])] = cols[rp[i]:rp[i + 1]]
+
+        self.join_queries(queries, eps, batch_bytes, HISS_OUT_CSR, True, take)
+        return res
+
+    def count_queries(self, queries, eps):
+        import torch
+        q = queries.contiguous()
+        out = torch.empty(q.shape[0], dtype=torch.int64, device="cuda")
+        _check(hiss_count_queries(self._h, q.data_ptr() if q.numel() else None, q.shape[0], float(eps),
+                                  out.data_ptr() if q.numel() else None), self._h, "hiss_count_queries")
+        return out
 
     def join_sets(self, eps, batch_bytes=0):
         """Full result as {query id: numpy array of neighbour ids}, through

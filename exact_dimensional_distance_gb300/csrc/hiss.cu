@@ -70,6 +70,10 @@ struct hiss_ctx {
     // test helpers
     DBuf t_keys_alt, t_vals_alt, t_sort_tmp, t_scan_tmp;
 
+    // semi-join query side
+    DBuf q_xv, q_xs, q_ids, q_cell_of_row, q_cell_start, q_cell_key, q_nbr, q_nbr_cnt, q_bound, q_work_key, q_cell_idx,
+        q_work;
+
     hiss_stats st{};
     cudaEvent_t ev[8] = {};
 };
@@ -349,12 +353,41 @@ void fill_grid_stats(hiss_ctx *ctx)
 
 namespace {
 
-// ---- query tiles in processing order (largest work first) ------------------------
-int ensure_tiles(hiss_ctx *ctx)
+// The query side of a join: query rows and ids (index order) and the query
+// cells with their stencils among the data's cells.  For the self-join it is
+// the data's own index; for the semi-join it is built from the queries.
+struct QuerySide {
+    const float *xq;
+    const int32_t *qids;
+    int64_t C;                  // query cells
+    const int32_t *qcell_start; // [C+1] first query row of each query cell
+    const int32_t *nbr;         // [C*27] data cells of each query cell's stencil
+    const int32_t *nbr_cnt;     // [C]
+    const int64_t *bound;       // [C] candidates of each query cell
+    const uint64_t *work_key;   // [C] ~(|cell| * bound)
+    const uint32_t *cell_idx;   // [C] 0 .. C-1
+};
+
+QuerySide self_side(hiss_ctx *ctx)
 {
-    if (ctx->tiles_valid) return HISS_OK;
+    QuerySide q;
+    q.xq = as<float>(ctx->xs);
+    q.qids = as<int32_t>(ctx->ids);
+    q.C = ctx->C;
+    q.qcell_start = as<int32_t>(ctx->cell_start);
+    q.nbr = as<int32_t>(ctx->nbr);
+    q.nbr_cnt = as<int32_t>(ctx->nbr_cnt);
+    q.bound = as<int64_t>(ctx->bound);
+    q.work_key = as<uint64_t>(ctx->work_key);
+    q.cell_idx = as<uint32_t>(ctx->cell_idx);
+    return q;
+}
+
+// ---- query tiles in processing order (largest work first) ------------------------
+int build_tiles(hiss_ctx *ctx, const QuerySide &qs)
+{
     cudaStream_t s = ctx->stream;
-    const int64_t C = ctx->C;
+    const int64_t C = qs.C;
     const int tq = refine_tq(ctx->d4), chunk = refine_chunk(ctx->d4);
     ST(ensure(ctx, ctx->lpt_keys, 8 * (size_t)C));
     ST(ensure(ctx, ctx->lpt_order, 4 * (size_t)C));
@@ -363,8 +396,8 @@ int ensure_tiles(hiss_ctx *ctx)
     ST(ensure(ctx, ctx->sort_tmp, sort_tmp_bytes(C)));
     ST(ensure(ctx, ctx->scan_tmp, 8 * (size_t)scan_tmp_elems(C + 1) + 64));
     // the work keys are consumed by the sort; copy them so the index stays intact
-    CK(cudaMemcpyAsync(ctx->lpt_keys.p, ctx->work_key.p, 8 * (size_t)C, cudaMemcpyDeviceToDevice, s));
-    CK(cudaMemcpyAsync(ctx->lpt_order.p, ctx->cell_idx.p, 4 * (size_t)C, cudaMemcpyDeviceToDevice, s));
+    CK(cudaMemcpyAsync(ctx->lpt_keys.p, qs.work_key, 8 * (size_t)C, cudaMemcpyDeviceToDevice, s));
+    CK(cudaMemcpyAsync(ctx->lpt_order.p, qs.cell_idx, 4 * (size_t)C, cudaMemcpyDeviceToDevice, s));
     int in_alt = 0;
     ST(ensure(ctx, ctx->keys_alt, 8 * (size_t)C));
     ST(ensure(ctx, ctx->vals_alt, 4 * (size_t)C));
@@ -379,7 +412,7 @@ int ensure_tiles(hiss_ctx *ctx)
     ctx->sorted_keys = nullptr;
     ctx->sorted_vals = nullptr;
 
-    CK(tile_counts(ctx->order, as<int32_t>(ctx->cell_start), C, tq, as<int32_t>(ctx->ntiles), s, &ctx->launches));
+    CK(tile_counts(ctx->order, qs.qcell_start, C, tq, as<int32_t>(ctx->ntiles), s, &ctx->launches));
     CK(scan_i32_to_i64(as<int32_t>(ctx->ntiles), as<int64_t>(ctx->tile_off), C, as<int64_t>(ctx->scan_tmp), s,
                        &ctx->launches));
     int64_t T = 0;
@@ -393,8 +426,8 @@ int ensure_tiles(hiss_ctx *ctx)
     ST(ensure(ctx, ctx->tile_unit, 8 * (size_t)(T + 1)));
     ST(ensure(ctx, ctx->tile_qoff, 8 * (size_t)(T + 1)));
     ST(ensure(ctx, ctx->scan_tmp, 8 * (size_t)scan_tmp_elems(T + 1) + 64));
-    CK(tile_fill(ctx->order, as<int32_t>(ctx->cell_start), as<int64_t>(ctx->bound), as<int64_t>(ctx->tile_off), C,
-                 tq, chunk, as<int32_t>(ctx->tile_cell), as<int32_t>(ctx->tile_q0), as<int32_t>(ctx->tile_nq),
+    CK(tile_fill(ctx->order, qs.qcell_start, qs.bound, as<int64_t>(ctx->tile_off), C, tq, chunk,
+                 as<int32_t>(ctx->tile_cell), as<int32_t>(ctx->tile_q0), as<int32_t>(ctx->tile_nq),
                  as<int64_t>(ctx->tile_word), as<int64_t>(ctx->tile_unit), s, &ctx->launches));
     CK(scan_i64(as<int64_t>(ctx->tile_word), as<int64_t>(ctx->tile_word), T, as<int64_t>(ctx->scan_tmp), s,
                 &ctx->launches));
@@ -409,6 +442,14 @@ int ensure_tiles(hiss_ctx *ctx)
     ctx->T = T;
     ctx->total_words = tot[0];
     ctx->total_units = tot[1];
+    return HISS_OK;
+}
+
+// Tiles of the self-join, cached with the index.
+int ensure_tiles(hiss_ctx *ctx)
+{
+    if (ctx->tiles_valid) return HISS_OK;
+    ST(build_tiles(ctx, self_side(ctx)));
     ctx->tiles_valid = true;
     return HISS_OK;
 }
@@ -430,24 +471,16 @@ int ensure_pinned(hiss_ctx *ctx, size_t bytes)
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
-int do_join(hiss_ctx *ctx, float eps, size_t batch_bytes, const hiss_out *out)
+// Plan the batches over the current tiles and run them: refinement,
+// compaction, delivery and the callback, batch by batch.
+int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_bytes, const hiss_out *out,
+                double ms_index, int64_t launches0)
 {
     const int mode = out ? out->mode : HISS_OUT_CSR;
-    if (mode != HISS_OUT_CSR && mode != HISS_OUT_MASK) return HISS_E_ARG;
     const int to_host = out ? out->copy_to_host : 0;
     hiss_batch_fn fn = out ? out->on_batch : nullptr;
     void *user = out ? out->user : nullptr;
     cudaStream_t s = ctx->stream;
-    const int64_t launches0 = ctx->launches;
-    double ms_index = 0.0;
-    if (!(ctx->grid_valid && ctx->grid_eps == eps)) {
-        ST(ensure_grid(ctx, eps));
-        ms_index = ctx->st.ms_index;
-    }
-    CK(cudaEventRecord(ctx->ev[2], s));
-    ST(ensure_tiles(ctx));
-    CK(cudaEventRecord(ctx->ev[3], s));
-
     if (batch_bytes == 0) {
         size_t fr = 0, tot = 0;
         CK(cudaMemGetInfo(&fr, &tot));
@@ -497,10 +530,11 @@ int do_join(hiss_ctx *ctx, float eps, size_t batch_bytes, const hiss_out *out)
         CK(cudaMemsetAsync(ctx->qcount.p, 0, 4 * (size_t)nq, s));
         RefineArgs ra{};
         ra.xs = as<float>(ctx->xs);
+        ra.xq = qs.xq;
         ra.cell_start = as<int32_t>(ctx->cell_start);
-        ra.nbr = as<int32_t>(ctx->nbr);
-        ra.nbr_cnt = as<int32_t>(ctx->nbr_cnt);
-        ra.bound = as<int64_t>(ctx->bound);
+        ra.nbr = qs.nbr;
+        ra.nbr_cnt = qs.nbr_cnt;
+        ra.bound = qs.bound;
         ra.tile_cell = as<int32_t>(ctx->tile_cell);
         ra.tile_q0 = as<int32_t>(ctx->tile_q0);
         ra.tile_nq = as<int32_t>(ctx->tile_nq);
@@ -525,6 +559,7 @@ int do_join(hiss_ctx *ctx, float eps, size_t batch_bytes, const hiss_out *out)
 
         CompactArgs ca{};
         ca.ids = as<int32_t>(ctx->ids);
+        ca.qids = qs.qids;
         ca.cell_start = ra.cell_start;
         ca.nbr = ra.nbr;
         ca.nbr_cnt = ra.nbr_cnt;
@@ -607,7 +642,6 @@ int do_join(hiss_ctx *ctx, float eps, size_t batch_bytes, const hiss_out *out)
         if (fn && fn(user, &hb) != 0) return HISS_E_CALLBACK;
     }
     ST(check_flags(ctx));
-    fill_grid_stats(ctx);
     ctx->st.pairs = mode == HISS_OUT_CSR ? pairs : -1;
     ctx->st.batches = nb;
     ctx->st.query_tiles = T;
@@ -621,6 +655,135 @@ int do_join(hiss_ctx *ctx, float eps, size_t batch_bytes, const hiss_out *out)
     ctx->st.ms_total = ms_index + ctx->st.ms_count + ms_refine + ms_compact + ms_deliver;
     ctx->st.kernel_launches = ctx->launches - launches0;
     return HISS_OK;
+}
+
+
+int do_join(hiss_ctx *ctx, float eps, size_t batch_bytes, const hiss_out *out)
+{
+    const int mode = out ? out->mode : HISS_OUT_CSR;
+    if (mode != HISS_OUT_CSR && mode != HISS_OUT_MASK) return HISS_E_ARG;
+    cudaStream_t s = ctx->stream;
+    const int64_t launches0 = ctx->launches;
+    double ms_index = 0.0;
+    if (!(ctx->grid_valid && ctx->grid_eps == eps)) {
+        ST(ensure_grid(ctx, eps));
+        ms_index = ctx->st.ms_index;
+    }
+    CK(cudaEventRecord(ctx->ev[2], s));
+    ST(ensure_tiles(ctx));
+    CK(cudaEventRecord(ctx->ev[3], s));
+    fill_grid_stats(ctx);
+    return run_batches(ctx, self_side(ctx), eps, batch_bytes, out, ms_index, launches0);
+}
+
+// ---- semi-join: the query side built from separate query points -------------------
+int build_query_side(hiss_ctx *ctx, const float *d_queries, int64_t nq, QuerySide *out)
+{
+    cudaStream_t s = ctx->stream;
+    const int d = ctx->d, d4 = ctx->d4;
+    ST(ensure(ctx, ctx->q_xv, sizeof(float) * (size_t)nq * d4));
+    ST(ensure(ctx, ctx->q_xs, sizeof(float) * (size_t)nq * d4));
+    ST(ensure(ctx, ctx->q_ids, 4 * (size_t)nq));
+    ST(ensure(ctx, ctx->q_cell_of_row, 4 * (size_t)nq));
+    ST(ensure(ctx, ctx->keys, 8 * (size_t)nq));
+    ST(ensure(ctx, ctx->vals, 4 * (size_t)nq));
+    ST(ensure(ctx, ctx->keys_alt, 8 * (size_t)nq));
+    ST(ensure(ctx, ctx->vals_alt, 4 * (size_t)nq));
+    ST(ensure(ctx, ctx->sort_tmp, sort_tmp_bytes(nq)));
+    ST(ensure(ctx, ctx->flag, 4 * (size_t)nq));
+    ST(ensure(ctx, ctx->flag_scan, 4 * (size_t)(nq + 1)));
+    ST(ensure(ctx, ctx->scan_tmp, 8 * (size_t)scan_tmp_elems(nq + 1) + 64));
+    CK(permute_pad(d_queries, nq, d, d4, as<int32_t>(ctx->perm_d), as<float>(ctx->q_xv), s, &ctx->launches));
+    int64_t cellmax = 0;
+    for (int k = 0; k < ctx->gp.ndim; ++k) {
+        const int dim = ctx->perm[k];
+        const double ext = ctx->stats[1 * (size_t)d + dim] - ctx->stats[0 * (size_t)d + dim];
+        cellmax = std::max(cellmax, (int64_t)std::floor(ext / ctx->gp.w));
+    }
+    CK(query_keys(as<float>(ctx->q_xv), nq, d4, ctx->gp, cellmax, as<uint64_t>(ctx->keys), as<uint32_t>(ctx->vals), s,
+                  &ctx->launches));
+    int in_alt = 0;
+    CK(sort_pairs(as<uint64_t>(ctx->keys), as<uint32_t>(ctx->vals), as<uint64_t>(ctx->keys_alt),
+                  as<uint32_t>(ctx->vals_alt), nq, 64, ctx->sort_tmp.p, as<int>(ctx->flags), s, &ctx->launches,
+                  &in_alt));
+    const uint64_t *skeys = in_alt ? as<uint64_t>(ctx->keys_alt) : as<uint64_t>(ctx->keys);
+    const uint32_t *svals = in_alt ? as<uint32_t>(ctx->vals_alt) : as<uint32_t>(ctx->vals);
+    CK(gather_rows(as<float>(ctx->q_xv), svals, nq, d4, as<float>(ctx->q_xs), as<int32_t>(ctx->q_ids), s,
+                   &ctx->launches));
+    CK(cell_flags(skeys, nq, 0, as<int32_t>(ctx->flag), s, &ctx->launches));
+    CK(scan_i32(as<int32_t>(ctx->flag), as<int32_t>(ctx->flag_scan), nq, as<int64_t>(ctx->scan_tmp), s,
+                &ctx->launches));
+    int32_t Cq32 = 0;
+    CK(cudaMemcpyAsync(&Cq32, as<int32_t>(ctx->flag_scan) + nq, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+    ST(sync(ctx));
+    ST(check_flags(ctx));
+    const int64_t Cq = Cq32;
+    ST(ensure(ctx, ctx->q_cell_start, 4 * (size_t)(Cq + 1)));
+    ST(ensure(ctx, ctx->q_cell_key, 8 * (size_t)Cq));
+    ST(ensure(ctx, ctx->q_nbr, 4 * (size_t)Cq * kStencil));
+    ST(ensure(ctx, ctx->q_nbr_cnt, 4 * (size_t)(Cq + 1)));
+    ST(ensure(ctx, ctx->q_bound, 8 * (size_t)(Cq + 1)));
+    ST(ensure(ctx, ctx->q_work_key, 8 * (size_t)Cq));
+    ST(ensure(ctx, ctx->q_cell_idx, 4 * (size_t)Cq));
+    ST(ensure(ctx, ctx->q_work, 8 * (size_t)(Cq + 1)));
+    CK(cell_starts(skeys, as<int32_t>(ctx->flag_scan), nq, 0, as<int32_t>(ctx->q_cell_start),
+                   as<uint64_t>(ctx->q_cell_key), as<int32_t>(ctx->q_cell_of_row), s, &ctx->launches));
+    CK(query_stencil(as<uint64_t>(ctx->q_cell_key), as<int32_t>(ctx->q_cell_start), Cq, as<uint64_t>(ctx->cell_key),
+                     as<int32_t>(ctx->cell_start), ctx->C, as<int32_t>(ctx->q_nbr), as<int32_t>(ctx->q_nbr_cnt),
+                     as<int64_t>(ctx->q_bound), as<uint64_t>(ctx->q_work_key), as<uint32_t>(ctx->q_cell_idx),
+                     as<int64_t>(ctx->q_work), s, &ctx->launches));
+    // candidates = sum over query cells of |cell| * bound
+    ST(ensure(ctx, ctx->sums2, 8 * (size_t)(Cq + 1)));
+    CK(scan_i64(as<int64_t>(ctx->q_work), as<int64_t>(ctx->sums2), Cq, as<int64_t>(ctx->scan_tmp), s, &ctx->launches));
+    int64_t cand = 0;
+    CK(cudaMemcpyAsync(&cand, as<int64_t>(ctx->sums2) + Cq, 8, cudaMemcpyDeviceToHost, s));
+    ST(sync(ctx));
+    ctx->st.candidates = cand;
+    QuerySide q;
+    q.xq = as<float>(ctx->q_xs);
+    q.qids = as<int32_t>(ctx->q_ids);
+    q.C = Cq;
+    q.qcell_start = as<int32_t>(ctx->q_cell_start);
+    q.nbr = as<int32_t>(ctx->q_nbr);
+    q.nbr_cnt = as<int32_t>(ctx->q_nbr_cnt);
+    q.bound = as<int64_t>(ctx->q_bound);
+    q.work_key = as<uint64_t>(ctx->q_work_key);
+    q.cell_idx = as<uint32_t>(ctx->q_cell_idx);
+    *out = q;
+    return HISS_OK;
+}
+
+int do_semi(hiss_ctx *ctx, const float *d_queries, int64_t nq, float eps, size_t batch_bytes, const hiss_out *out,
+            int64_t *d_counts)
+{
+    const int mode = out ? out->mode : HISS_OUT_CSR;
+    if (mode != HISS_OUT_CSR && mode != HISS_OUT_MASK) return HISS_E_ARG;
+    cudaStream_t s = ctx->stream;
+    const int64_t launches0 = ctx->launches;
+    double ms_index = 0.0;
+    if (!(ctx->grid_valid && ctx->grid_eps == eps)) {
+        ST(ensure_grid(ctx, eps));
+        ms_index = ctx->st.ms_index;
+    }
+    fill_grid_stats(ctx);
+    ctx->st.pairs = 0;
+    ctx->st.batches = 0;
+    if (nq == 0) return HISS_OK;
+    CK(cudaEventRecord(ctx->ev[2], s));
+    QuerySide qs;
+    ST(build_query_side(ctx, d_queries, nq, &qs));
+    if (d_counts) {
+        CK(scatter_counts(qs.qids, as<int32_t>(ctx->q_cell_of_row), qs.bound, nq, d_counts, s, &ctx->launches));
+        CK(cudaEventRecord(ctx->ev[3], s));
+        ST(sync(ctx));
+        ctx->st.ms_count = elapsed(ctx, 2, 3);
+        ctx->st.kernel_launches = ctx->launches - launches0;
+        return HISS_OK;
+    }
+    ctx->tiles_valid = false;  // the tile arrays now describe the queries
+    ST(build_tiles(ctx, qs));
+    CK(cudaEventRecord(ctx->ev[3], s));
+    return run_batches(ctx, qs, eps, batch_bytes, out, ms_index, launches0);
 }
 
 }  // namespace
@@ -668,7 +831,9 @@ void hiss_destroy(hiss_ctx *ctx)
                    &ctx->tile_q0, &ctx->tile_nq, &ctx->tile_word, &ctx->tile_unit, &ctx->tile_qoff,
                    &ctx->boundaries, &ctx->binfo, &ctx->nb_d, &ctx->mask, &ctx->qcount, &ctx->row_ptr, &ctx->cols,
                    &ctx->query_ids, &ctx->query_rows, &ctx->cand, &ctx->mask_row_ptr, &ctx->t_keys_alt,
-                   &ctx->t_vals_alt, &ctx->t_sort_tmp, &ctx->t_scan_tmp};
+                   &ctx->t_vals_alt, &ctx->t_sort_tmp, &ctx->t_scan_tmp, &ctx->q_xv, &ctx->q_xs, &ctx->q_ids,
+                   &ctx->q_cell_of_row, &ctx->q_cell_start, &ctx->q_cell_key, &ctx->q_nbr, &ctx->q_nbr_cnt,
+                   &ctx->q_bound, &ctx->q_work_key, &ctx->q_cell_idx, &ctx->q_work};
     for (DBuf *b : all) release(ctx, *b);
     cudaStreamSynchronize(ctx->stream);
     if (ctx->h_pinned) cudaFreeHost(ctx->h_pinned);
@@ -722,6 +887,25 @@ int hiss_join(hiss_ctx *ctx, float eps, size_t batch_bytes, const hiss_out *out)
     return do_join(ctx, eps, batch_bytes, out);
 }
 
+int hiss_join_queries(hiss_ctx *ctx, const float *d_queries, int64_t nq, float eps, size_t batch_bytes,
+                      const hiss_out *out)
+{
+    ST(enter(ctx));
+    if (!ctx->built) return HISS_E_STATE;
+    if (nq < 0 || nq >= (int64_t(1) << 30) || (nq > 0 && !d_queries)) return HISS_E_ARG;
+    if (!(eps >= 0.0f) || std::isinf(eps)) return HISS_E_ARG;
+    return do_semi(ctx, d_queries, nq, eps, batch_bytes, out, nullptr);
+}
+
+int hiss_count_queries(hiss_ctx *ctx, const float *d_queries, int64_t nq, float eps, int64_t *d_counts)
+{
+    ST(enter(ctx));
+    if (!ctx->built) return HISS_E_STATE;
+    if (nq < 0 || nq >= (int64_t(1) << 30) || (nq > 0 && (!d_queries || !d_counts))) return HISS_E_ARG;
+    if (!(eps >= 0.0f) || std::isinf(eps)) return HISS_E_ARG;
+    return do_semi(ctx, d_queries, nq, eps, 0, nullptr, d_counts);
+}
+
 int hiss_work_profile(hiss_ctx *ctx, float eps, int64_t *out)
 {
     ST(enter(ctx));
@@ -734,6 +918,7 @@ int hiss_work_profile(hiss_ctx *ctx, float eps, int64_t *out)
     CK(cudaMemsetAsync(ctx->nb_d.p, 0, 16, ctx->stream));
     RefineArgs ra{};
     ra.xs = as<float>(ctx->xs);
+    ra.xq = as<float>(ctx->xs);
     ra.cell_start = as<int32_t>(ctx->cell_start);
     ra.nbr = as<int32_t>(ctx->nbr);
     ra.nbr_cnt = as<int32_t>(ctx->nbr_cnt);

@@ -69,6 +69,13 @@ cudaError_t cell_starts(const uint64_t *keys, const int32_t *flag_scan, int64_t 
 cudaError_t stencil(const uint64_t *cell_key, const int32_t *cell_start, int64_t C, int32_t *nbr, int32_t *nbr_cnt,
                     int64_t *bound, uint64_t *work_key, uint32_t *cell_idx, int64_t *work, cudaStream_t s,
                     int64_t *launches);
+// Semi-join: queries keyed into the data's grid (see k_query_keys) and the
+// stencil of each query cell among the data's cells.
+cudaError_t query_keys(const float *xv, int64_t n, int d4, GridParams gp, int64_t cellmax, uint64_t *keys,
+                       uint32_t *vals, cudaStream_t s, int64_t *launches);
+cudaError_t query_stencil(const uint64_t *qcell_key, const int32_t *qcell_start, int64_t Cq, const uint64_t *cell_key,
+                          const int32_t *cell_start, int64_t C, int32_t *nbr, int32_t *nbr_cnt, int64_t *bound,
+                          uint64_t *work_key, uint32_t *cell_idx, int64_t *work, cudaStream_t s, int64_t *launches);
 cudaError_t scatter_counts(const int32_t *ids, const int32_t *cell_of_row, const int64_t *bound, int64_t n,
                            int64_t *counts, cudaStream_t s, int64_t *launches);
 // Per cell in processing order: tiles and their sizes.
@@ -89,6 +96,7 @@ cudaError_t plan_batches(const int64_t *tile_word_off, const int64_t *tile_unit,
 // ---- refinement and compaction (refine.cu) ---------------------------------
 struct RefineArgs {
     const float *xs;            // index-ordered points, n x d4 (row stride d4)
+    const float *xq;            // query rows (== xs for the self-join)
     const int32_t *cell_start;  // [C+1]
     const int32_t *nbr;         // [C*27]
     const int32_t *nbr_cnt;     // [C]
@@ -116,6 +124,7 @@ cudaError_t refine_profile(const RefineArgs &a, cudaStream_t s, int64_t *launche
 
 struct CompactArgs {
     const int32_t *ids;         // [n] original id per index row
+    const int32_t *qids;        // original id per query row (== ids for the self-join)
     const int32_t *cell_start;
     const int32_t *nbr;
     const int32_t *nbr_cnt;

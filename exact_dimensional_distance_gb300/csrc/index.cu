@@ -234,6 +234,75 @@ __global__ void k_stencil(const uint64_t *__restrict__ cell_key, const int32_t *
     cell_idx[c] = (uint32_t)c;
 }
 
+// Semi-join: key each query into the data's grid.  Cell coordinates are
+// signed; a query more than one cell outside the grid on some index dimension
+// has no candidate and gets the key ~0 (it sorts last).  Otherwise the key is
+// the Morton key of the coordinates shifted by +1 (so -1 maps to 0).
+__global__ void k_query_keys(const float *__restrict__ xv, int64_t n, int d4, GridParams gp, int64_t cellmax,
+                             uint64_t *__restrict__ keys, uint32_t *__restrict__ vals)
+{
+    const int64_t i = (int64_t)blockIdx.x * kT + threadIdx.x;
+    if (i >= n) return;
+    uint64_t key = 0;
+    bool outside = false;
+    for (int k = 0; k < 3; ++k) {
+        int64_t c = 0;
+        if (k < gp.ndim) {
+            const double u = ((double)xv[i * d4 + k] - gp.origin[k]) / gp.w;
+            const double f = floor(u);
+            if (f < -1.0 || f > (double)(cellmax + 1)) outside = true;
+            else c = (int64_t)f;
+        }
+        key |= spread3((uint64_t)(c + 1)) << k;
+    }
+    keys[i] = outside ? ~0ull : key;
+    vals[i] = (uint32_t)i;
+}
+
+// Stencil of each query cell in the data's grid (cells of D around it, order
+// dz, dy, dx), its candidate count and work, as k_stencil does for D's cells.
+__global__ void k_query_stencil(const uint64_t *__restrict__ qcell_key, const int32_t *__restrict__ qcell_start,
+                                int64_t Cq, const uint64_t *__restrict__ cell_key,
+                                const int32_t *__restrict__ cell_start, int64_t C, int32_t *__restrict__ nbr,
+                                int32_t *__restrict__ nbr_cnt, int64_t *__restrict__ bound,
+                                uint64_t *__restrict__ work_key, uint32_t *__restrict__ cell_idx,
+                                int64_t *__restrict__ work)
+{
+    const int64_t c = (int64_t)blockIdx.x * kT + threadIdx.x;
+    if (c >= Cq) return;
+    const uint64_t key = qcell_key[c];
+    int cnt = 0;
+    int64_t b = 0;
+    if (key != ~0ull) {
+        const int64_t cx = (int64_t)compact3(key) - 1, cy = (int64_t)compact3(key >> 1) - 1,
+                      cz = (int64_t)compact3(key >> 2) - 1;
+        const int64_t lim = 1 << 21;
+        for (int dz = -1; dz <= 1; ++dz)
+            for (int dy = -1; dy <= 1; ++dy)
+                for (int dx = -1; dx <= 1; ++dx) {
+                    const int64_t a0 = cx + dx, a1 = cy + dy, a2 = cz + dz;
+                    if (a0 < 0 || a1 < 0 || a2 < 0 || a0 >= lim || a1 >= lim || a2 >= lim) continue;
+                    const uint64_t nk =
+                        spread3((uint64_t)a0) | (spread3((uint64_t)a1) << 1) | (spread3((uint64_t)a2) << 2);
+                    int64_t lo = 0, hi = C;
+                    while (lo < hi) {
+                        const int64_t mid = (lo + hi) >> 1;
+                        if (cell_key[mid] < nk) lo = mid + 1; else hi = mid;
+                    }
+                    if (lo < C && cell_key[lo] == nk) {
+                        nbr[c * kStencil + cnt++] = (int32_t)lo;
+                        b += cell_start[lo + 1] - cell_start[lo];
+                    }
+                }
+    }
+    nbr_cnt[c] = cnt;
+    bound[c] = b;
+    const int64_t w = (int64_t)(qcell_start[c + 1] - qcell_start[c]) * b;
+    work[c] = w;
+    work_key[c] = ~(uint64_t)w;
+    cell_idx[c] = (uint32_t)c;
+}
+
 __global__ void k_scatter_counts(const int32_t *__restrict__ ids, const int32_t *__restrict__ cell_of_row,
                                  const int64_t *__restrict__ bound, int64_t n, int64_t *__restrict__ counts)
 {
@@ -377,6 +446,24 @@ cudaError_t stencil(const uint64_t *cell_key, const int32_t *cell_start, int64_t
                     int64_t *launches)
 {
     k_stencil<<<blocks_for(C), kT, 0, s>>>(cell_key, cell_start, C, nbr, nbr_cnt, bound, work_key, cell_idx, work);
+    ++*launches;
+    return cudaGetLastError();
+}
+
+cudaError_t query_keys(const float *xv, int64_t n, int d4, GridParams gp, int64_t cellmax, uint64_t *keys,
+                       uint32_t *vals, cudaStream_t s, int64_t *launches)
+{
+    k_query_keys<<<blocks_for(n), kT, 0, s>>>(xv, n, d4, gp, cellmax, keys, vals);
+    ++*launches;
+    return cudaGetLastError();
+}
+
+cudaError_t query_stencil(const uint64_t *qcell_key, const int32_t *qcell_start, int64_t Cq, const uint64_t *cell_key,
+                          const int32_t *cell_start, int64_t C, int32_t *nbr, int32_t *nbr_cnt, int64_t *bound,
+                          uint64_t *work_key, uint32_t *cell_idx, int64_t *work, cudaStream_t s, int64_t *launches)
+{
+    k_query_stencil<<<blocks_for(Cq), kT, 0, s>>>(qcell_key, qcell_start, Cq, cell_key, cell_start, C, nbr, nbr_cnt,
+                                                  bound, work_key, cell_idx, work);
     ++*launches;
     return cudaGetLastError();
 }

@@ -209,8 +209,8 @@ __global__ void __launch_bounds__(kThreads, HISS_REFINE_MINB) k_refine(const Ref
         const int pid = idx / C4, cc = idx - pid * C4;
         const int ra = 8 * (pid >> 2) + (pid & 3), rb = ra + 4;
         const float4 inf4 = make_float4(INFINITY, INFINITY, INFINITY, INFINITY);
-        const float4 x = ra < nq ? *reinterpret_cast<const float4 *>(a.xs + (int64_t)(q0 + ra) * d4 + 4 * cc) : inf4;
-        const float4 y = rb < nq ? *reinterpret_cast<const float4 *>(a.xs + (int64_t)(q0 + rb) * d4 + 4 * cc) : inf4;
+        const float4 x = ra < nq ? *reinterpret_cast<const float4 *>(a.xq + (int64_t)(q0 + ra) * d4 + 4 * cc) : inf4;
+        const float4 y = rb < nq ? *reinterpret_cast<const float4 *>(a.xq + (int64_t)(q0 + rb) * d4 + 4 * cc) : inf4;
         float4 *dst = reinterpret_cast<float4 *>(Q2 + pid * S2 + 8 * cc);
         dst[0] = make_float4(x.x, y.x, x.y, y.y);
         dst[1] = make_float4(x.z, y.z, x.w, y.w);
@@ -432,7 +432,7 @@ __global__ void __launch_bounds__(kCompactWarps * 32) k_compact(const CompactArg
     const int64_t W4 = (W + 3) & ~int64_t(3);
     const int64_t woff = a.tile_word[t] - a.word0 + i * W4;
     if (lane == 0) {
-        a.query_ids[gq] = a.ids[row];
+        a.query_ids[gq] = a.qids[row];
         a.query_rows[gq] = row;
         if (a.cand) a.cand[gq] = B;
         if (a.mask_row_ptr) {

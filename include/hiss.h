@@ -149,6 +149,26 @@ typedef struct {
  * cell's points in index order. */
 int hiss_join(hiss_ctx *ctx, float eps, size_t batch_bytes, const hiss_out *out);
 
+/* Semi-join (RT-HiSS Section II-A: "D and Q are distinct"; the method
+ * applies unchanged): for each of nq query points (d_queries: device pointer,
+ * nq x d float32 row-major, same d as the dataset, read only during the call)
+ * every point of the dataset within eps, inclusive.  The queries are keyed
+ * into the dataset's grid for eps (built or reused as by hiss_count); a query
+ * more than one cell outside the grid on an index dimension has no candidate
+ * and an empty row.  Batches, output modes and the callback are those of
+ * hiss_join, with query_ids = row indices of d_queries (0 .. nq-1) and
+ * query_rows = rows of the queries in their own cell order; cols are dataset
+ * ids.  No query is its own neighbour unless it coincides with a data point
+ * within eps.  nq = 0 is valid (no batch).  Invalidates the self-join's
+ * cached tiles (the next hiss_join rebuilds them). */
+int hiss_join_queries(hiss_ctx *ctx, const float *d_queries, int64_t nq, float eps, size_t batch_bytes,
+                      const hiss_out *out);
+
+/* Count bound of the semi-join: d_counts (device int64[nq], query order)
+ * receives, per query, the number of dataset points in the 27 grid cells
+ * around the query's cell, >= its true neighbour count. */
+int hiss_count_queries(hiss_ctx *ctx, const float *d_queries, int64_t nq, float eps, int64_t *d_counts);
+
 /* Read-only view of the index built for the last eps (device pointers owned
  * by the context, valid until the next build or a call with another eps). */
 typedef struct {

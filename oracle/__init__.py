@@ -61,6 +61,8 @@ def _lib():
         lib.orc_rows_fill.argtypes = [p, i64, i32, f64, f64, p, i64, p, p, p, p]
         lib.orc_counts.argtypes = [p, i64, i32, f64, p]
         lib.orc_pick_eps2.argtypes = [p, i64, i32, p, i64, i64, i64, p, p]
+        lib.orc_semi_count.argtypes = [p, i64, p, i64, i32, f64, f64, p]
+        lib.orc_semi_fill.argtypes = [p, i64, p, i64, i32, f64, f64, p, p, p, p]
         lib.orc_pick_eps2.restype = ctypes.c_int
         _lib_handle = lib
     return _lib_handle
@@ -120,6 +122,88 @@ def rows(x, eps, query_rows, band: float = BAND):
     lib.orc_rows_fill(_ptr(x), x.shape[0], x.shape[1], e2, float(band), _ptr(q), q.size,
                       _ptr(row_ptr), _ptr(cols), _ptr(flag), _ptr(dist2))
     return row_ptr, cols[:nnz], flag[:nnz], dist2[:nnz]
+
+
+def semi_rows(xq, xd, eps, band: float = BAND):
+    """Semi-join rows (RT-HiSS Section II-A, Q distinct from D): for each
+    query q_r, every j of D with s(q_r, p_j) <= eps^2 (1 + band), increasing;
+    returns (row_ptr, cols, flag, dist2) as ``rows`` does."""
+    xq = _points(xq)
+    xd = _points(xd)
+    if xq.shape[1] != xd.shape[1]:
+        raise ValueError("queries and data must have the same dimension")
+    lib = _lib()
+    e2 = eps_squared(eps)
+    cnt = np.empty(xq.shape[0], dtype=np.int64)
+    lib.orc_semi_count(_ptr(xq), xq.shape[0], _ptr(xd), xd.shape[0], xd.shape[1], e2, float(band), _ptr(cnt))
+    row_ptr = np.zeros(xq.shape[0] + 1, dtype=np.int64)
+    np.cumsum(cnt, out=row_ptr[1:])
+    nnz = int(row_ptr[-1])
+    cols = np.empty(max(nnz, 1), dtype=np.int32)
+    flag = np.empty(max(nnz, 1), dtype=np.uint8)
+    dist2 = np.empty(max(nnz, 1), dtype=np.float64)
+    lib.orc_semi_fill(_ptr(xq), xq.shape[0], _ptr(xd), xd.shape[0], xd.shape[1], e2, float(band), _ptr(row_ptr),
+                      _ptr(cols), _ptr(flag), _ptr(dist2))
+    return row_ptr, cols[:nnz], flag[:nnz], dist2[:nnz]
+
+
+def semi_row_sets(xq, xd, eps, band: float = BAND):
+    """Per query: (certain neighbours in D, band pairs) as two sets."""
+    row_ptr, cols, flag, _ = semi_rows(xq, xd, eps, band)
+    out = []
+    for r in range(len(row_ptr) - 1):
+        c = cols[row_ptr[r]:row_ptr[r + 1]]
+        f = flag[row_ptr[r]:row_ptr[r + 1]]
+        out.append((set(c[f == 0].tolist()), set(c[f == 1].tolist())))
+    return out
+
+
+def semi_brute_force_py(xq, xd, eps) -> list:
+    """The semi-join definition as nested pure-Python loops (tiny inputs)."""
+    xq = _points(xq)
+    xd = _points(xd)
+    e2 = eps_squared(eps)
+    res = []
+    for q in xq.tolist():
+        row = set()
+        for j, p in enumerate(xd.tolist()):
+            s = 0.0
+            for a, b in zip(q, p):
+                t = a - b
+                s += t * t
+            if s <= e2:
+                row.add(j)
+        res.append(row)
+    return res
+
+
+def semi_count_bound(xq, xd, eps) -> np.ndarray:
+    """Semi-join count bound: points of D in the 27 grid cells of D's grid
+    around each query's cell (the query keyed into D's grid, cell coordinates
+    taken as signed integers; a query more than one cell outside D's grid has
+    no candidate)."""
+    xq = _points(xq)
+    xd = _points(xd)
+    g = grid(xd, eps)
+    idx = g["perm"][: min(3, xd.shape[1])]
+    w = g["w"]
+    cq = np.zeros((xq.shape[0], 3), dtype=np.int64)
+    for k in range(idx.size):
+        u = (xq[:, idx[k]].astype(np.float64) - g["origin"][k]) / w
+        cq[:, k] = np.floor(u).astype(np.int64)
+    ck = g["cell_key"]
+    size = np.diff(g["cell_start"])
+    table = {int(k): int(s) for k, s in zip(ck.tolist(), size.tolist())}
+    out = np.zeros(xq.shape[0], dtype=np.int64)
+    for r in range(xq.shape[0]):
+        tot = 0
+        for dx, dy, dz in STENCIL:
+            a, b, c = cq[r, 0] + dx, cq[r, 1] + dy, cq[r, 2] + dz
+            if min(a, b, c) < 0 or max(a, b, c) >= (1 << 21):
+                continue
+            tot += table.get(int(morton3(np.uint64(a), np.uint64(b), np.uint64(c))), 0)
+        out[r] = tot
+    return out
 
 
 def row_sets(x, eps, query_rows, band: float = BAND):

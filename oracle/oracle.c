@@ -84,6 +84,49 @@ void orc_rows_fill(const float *x, int64_t n, int32_t d, double eps2, double ban
     }
 }
 
+/*
+ * Semi-join (RT-HiSS Section II-A: "D and Q are distinct"): for each query
+ * row r of xq (nq x d), count the points j of xd (nd x d) with
+ * s(q_r, p_j) <= eps2 * (1 + band); then list them (increasing j) with the
+ * same band flags as orc_rows_fill.  No point is implicitly its own
+ * neighbour: only distances count.
+ */
+void orc_semi_count(const float *xq, int64_t nq, const float *xd, int64_t nd, int32_t d, double eps2,
+                    double band, int64_t *out_count)
+{
+    const double hi = eps2 * (1.0 + band);
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t r = 0; r < nq; ++r) {
+        const float *q = xq + r * (int64_t)d;
+        int64_t c = 0;
+        for (int64_t j = 0; j < nd; ++j)
+            if (sqdist(q, xd + j * (int64_t)d, d) <= hi)
+                ++c;
+        out_count[r] = c;
+    }
+}
+
+void orc_semi_fill(const float *xq, int64_t nq, const float *xd, int64_t nd, int32_t d, double eps2,
+                   double band, const int64_t *row_ptr, int32_t *cols, uint8_t *flag, double *dist2)
+{
+    const double hi = eps2 * (1.0 + band);
+    const double lo = eps2 * (1.0 - band);
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t r = 0; r < nq; ++r) {
+        const float *q = xq + r * (int64_t)d;
+        int64_t o = row_ptr[r];
+        for (int64_t j = 0; j < nd; ++j) {
+            double s = sqdist(q, xd + j * (int64_t)d, d);
+            if (s <= hi) {
+                cols[o] = (int32_t)j;
+                flag[o] = (uint8_t)(s >= lo);
+                dist2[o] = s;
+                ++o;
+            }
+        }
+    }
+}
+
 /* Exact neighbour count of every point (band = 0), rows 0..n-1. */
 void orc_counts(const float *x, int64_t n, int32_t d, double eps2, int64_t *out_count)
 {

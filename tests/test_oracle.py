@@ -216,3 +216,33 @@ def test_grid_neighbours_within_one_cell():
     for i, row in enumerate(_sets(x, eps)):
         for j in row:
             assert np.max(np.abs(cells[i] - cells[j])) <= 1
+
+
+# ---------------- semi-join (Q distinct from D) -----------------------------
+
+def test_semi_join_hand_case():
+    xd = np.array([[0.0, 0.0], [3.0, 4.0], [10.0, 0.0]], dtype=np.float32)
+    xq = np.array([[0.0, 0.0], [6.0, 8.0], [13.0, 4.0], [50.0, 50.0]], dtype=np.float32)
+    row_ptr, cols, _, _ = oracle.semi_rows(xq, xd, 5.0, band=0.0)
+    rows = [sorted(cols[row_ptr[i]:row_ptr[i + 1]].tolist()) for i in range(4)]
+    assert rows == [[0, 1], [1], [2], []]          # |(6,8)-(3,4)| = 5 inclusive; (13,4)-(10,0) = 5
+    assert oracle.semi_brute_force_py(xq, xd, 5.0) == [{0, 1}, {1}, {2}, set()]
+
+
+def test_semi_join_with_q_equal_d_is_self_join():
+    x = datagen.generate(1, n=600)
+    a = oracle.semi_rows(x, x, 0.5, band=0.0)
+    b = oracle.rows(x, 0.5, np.arange(len(x)), band=0.0)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_semi_join_matches_plain_loops_and_bound_covers():
+    rng = np.random.default_rng(5)
+    xd = rng.random((300, 5)).astype(np.float32)
+    xq = (rng.random((120, 5)) * 1.4 - 0.2).astype(np.float32)   # some queries outside D's box
+    eps = 0.35
+    row_ptr, cols, _, _ = oracle.semi_rows(xq, xd, eps, band=0.0)
+    got = [set(cols[row_ptr[i]:row_ptr[i + 1]].tolist()) for i in range(len(xq))]
+    assert got == oracle.semi_brute_force_py(xq, xd, eps)
+    bound = oracle.semi_count_bound(xq, xd, eps)
+    assert all(bound[i] >= len(got[i]) for i in range(len(xq)))
