@@ -173,6 +173,11 @@ int check_flags(hiss_ctx *ctx)
         ctx->sticky = HISS_E_CUDA;
         return HISS_E_CUDA;
     }
+    if (h[kFlagRefineTimeout]) {
+        snprintf(ctx->cuda_err, sizeof(ctx->cuda_err), "refinement stage wait exceeded its limit");
+        ctx->sticky = HISS_E_CUDA;
+        return HISS_E_CUDA;
+    }
     return HISS_OK;
 }
 
@@ -553,6 +558,7 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
         ra.d = ctx->d;
         ra.eps2 = eps * eps;
         ra.prof = nullptr;
+        ra.flags = as<int>(ctx->flags);
         CK(cudaEventRecord(ctx->ev[4], s));
         CK(refine(ra, s, &ctx->launches));
         CK(cudaEventRecord(ctx->ev[5], s));
@@ -937,9 +943,11 @@ int hiss_work_profile(hiss_ctx *ctx, float eps, int64_t *out)
     ra.d = ctx->d;
     ra.eps2 = eps * eps;
     ra.prof = as<int64_t>(ctx->nb_d);
+    ra.flags = as<int>(ctx->flags);
     CK(refine_profile(ra, ctx->stream, &ctx->launches));
     CK(cudaMemcpyAsync(out, ctx->nb_d.p, 16, cudaMemcpyDeviceToHost, ctx->stream));
-    return sync(ctx);
+    ST(sync(ctx));
+    return check_flags(ctx);
 }
 
 int hiss_index(hiss_ctx *ctx, hiss_index_view *v)

@@ -10,14 +10,12 @@
 namespace hiss {
 
 // ---- tiling of the refinement kernel ---------------------------------------
-// A refinement unit is one query tile (up to TQ queries of one cell) against
-// one chunk of up to kChunkTiles * TP of the cell's stencil candidates.
-constexpr int kThreads = 256;
-constexpr int kChunkTiles = 64;
+// A refinement unit is one query tile (up to refine_tq() queries of one cell)
+// against one chunk of up to refine_chunk() of the cell's stencil candidates.
 constexpr int kStencil = 27;
 
 // Device-side error flags (one int each in ctx->d_flags).
-enum { kFlagSortTimeout = 0, kFlagPlanTooSmall = 1, kFlagOverflow = 2, kNumFlags = 4 };
+enum { kFlagSortTimeout = 0, kFlagPlanTooSmall = 1, kFlagOverflow = 2, kFlagRefineTimeout = 3, kNumFlags = 4 };
 
 // Sticky-error launch check used by every host wrapper.
 #define HISS_TRY(expr)                                      \
@@ -116,6 +114,7 @@ struct RefineArgs {
     int d;                      // true dimension (profile mode caps the last step at d)
     float eps2;
     int64_t *prof;              // profile mode: [2] counters (sum of per-pair exit dims, executed dims)
+    int *flags;                 // device int[kNumFlags]; kFlagRefineTimeout set if a stage wait gave up
 };
 int refine_tq(int d4);
 int refine_chunk(int d4);

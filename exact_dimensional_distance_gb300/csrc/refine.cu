@@ -4,47 +4,70 @@
 // One thread block refines one unit: a tile of up to TQ queries of one grid
 // cell against one chunk of the cell's stencil candidates (the cells around
 // it, concatenated in stencil order).  The query tile stays in shared memory
-// (two query rows interleaved per pair row); candidate tiles of TP points are
-// staged through shared memory with cp.async, double-buffered, gathered row by
-// row from the stencil cells.  Each thread owns an MQ x MP block of (query,
-// candidate) squared distances, held as packed float32 pairs, and adds two
-// dimensions per step with f32x2 subtract / multiply-add instructions (one
-// instruction per pair and dimension instead of two).  Dimensions are in
-// variance order, so after 4, 8 and 12 dimensions and then every 8 a warp checks
+// (two query rows interleaved per pair row).  A producer warp streams the
+// candidates through a ring of shared-memory stages, gathering each candidate
+// row from its stencil cell with cp.async, completion tracked by mbarriers.
+// Each compute thread owns an 8 x 4 block of (query, candidate) squared
+// distances (4 x 4 above 64 dimensions), held as packed float32 pairs, and
+// adds two dimensions per step with f32x2 subtract / multiply-add
+// instructions (one instruction per pair and dimension instead of two).
+// Dimensions are in variance order, so after every 4 dimensions a warp checks
 // whether all of its partial sums already exceed eps^2 and, if so, leaves the
-// tile (early termination, Section IV-A).  The result is one bit per pair,
-// sum <= eps^2, written to the query's mask row; the popcount of each word is
-// accumulated into the query's neighbour count.
+// tile (early termination, Section IV-A).  The result is one bit per pair, sum <= eps^2,
+// written to the query's mask row; the popcount of each word is accumulated
+// into the query's neighbour count.
 #include "hiss_internal.cuh"
 
 namespace hiss {
 namespace {
 
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
-{
-    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
-
-// Row stride of a staged tile, in floats: d4 plus padding chosen so that
-// stride / 4 is odd, which makes the 16-byte loads of 8 consecutive rows hit
-// 8 distinct bank quads.
+// ---- staging geometry ---------------------------------------------------------
+// Row stride of a staged candidate tile, in floats: d4 plus padding chosen so
+// that stride / 4 is odd, which makes the 8-byte loads of 8 consecutive rows
+// hit 8 distinct bank quads.
 __host__ __device__ __forceinline__ int tile_stride(int d4) { return ((d4 / 4) % 2 == 0) ? d4 + 4 : d4 + 8; }
 
-template <int MQ, int MP>
-struct Tile {
-    static constexpr int TQ = 16 * MQ;   // 4 warps x 4 lanes x MQ queries
-    static constexpr int TP = 16 * MP;   // 2 warps x 8 lanes x MP candidates
-    static constexpr int CH = kChunkTiles * TP;
-    static constexpr int WPW = MP / 4;   // mask words per query row per warp column
-};
+// Row stride of the pair-interleaved query tile, in floats: 2 d4 + 4, so that
+// stride / 4 is odd (4 consecutive pair rows hit distinct bank quads).
+__host__ __device__ __forceinline__ int pair_stride(int d4) { return 2 * d4 + 4; }
 
-// Row stride of the pair-interleaved query tile, in floats: 2 d4 plus padding
-// so that stride / 4 is odd (4 consecutive pair rows hit distinct bank quads).
-__host__ __device__ __forceinline__ int pair_stride(int d4) { return (d4 % 8 == 0) ? 2 * d4 + 4 : 2 * d4 + 8; }
+// Thread-block shape of the refinement.  Eight compute warps (4 query warps x
+// 2 candidate warps) and one producer warp.  A compute warp owns a 4 MQ x 32
+// block of (query, candidate) pairs of the staged tile; each of its threads
+// owns MQ x MP of them.
+constexpr int kQueryWarps = 4, kCandWarps = 2;
+constexpr int kComputeWarps = kQueryWarps * kCandWarps;
+constexpr int kComputeThreads = kComputeWarps * 32;
+constexpr int kRefineThreads = kComputeThreads + 32;
+constexpr int kCH = 8192;  // candidates per unit
+
+// Per-thread block MQ x MP: 8 x 4 up to d4 = 64 (tiles of 128 queries x 64
+// candidates), 4 x 4 above (64 x 64), so that two blocks fit per SM.
+template <int MQ, int MP>
+struct Geo {
+    static constexpr int TQ = kQueryWarps * 4 * MQ;  // queries per tile
+    static constexpr int TP = kCandWarps * 8 * MP;   // candidates per staged tile
+};
+constexpr int kMaxStages = 4;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a stage wait gives up after 2 s
+
+// Stages of the candidate ring: as many as fit (up to 4, at least 2) in
+// about a third of the SM's shared memory, so that two or three blocks stay
+// resident per SM.
+template <int MQ, int MP>
+__host__ __device__ __forceinline__ int refine_stages(int d4)
+{
+    const int q2 = (Geo<MQ, MP>::TQ / 2) * pair_stride(d4) * 4, stage = Geo<MQ, MP>::TP * tile_stride(d4) * 4;
+    int ns = (75 * 1024 - q2) / stage;
+    return ns < 2 ? 2 : (ns > kMaxStages ? kMaxStages : ns);
+}
+template <int MQ, int MP>
+__host__ __forceinline__ size_t refine_smem(int d4)
+{
+    using G = Geo<MQ, MP>;
+    return sizeof(float) *
+           ((size_t)(G::TQ / 2) * pair_stride(d4) + (size_t)refine_stages<MQ, MP>(d4) * G::TP * tile_stride(d4));
+}
 
 // Packed float32 pairs (two lanes of one 64-bit register), computed with the
 // sm_100-family f32x2 instructions: each is two independent round-to-nearest
@@ -90,11 +113,73 @@ __device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c)
     return r;
 }
 
+// ---- mbarrier and asynchronous-copy primitives (inline PTX) ---------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+                     smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Wait for the phase of the given parity to complete.  Gives up (returns
+// false) after kWaitLimitNs, so a logic error can never hang the GPU.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+// 16-byte asynchronous copy global -> shared (L1 bypass).
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+// Make the mbarrier track completion of all cp.async issued so far by this
+// thread: the pending count is raised now and lowered when they complete.
+__device__ __forceinline__ void cp_async_arrive_on(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void compute_warps_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kComputeThreads) : "memory");
+}
+
 // The thread's MQ x MP block of squared distances is held as MQ/2 x MP
 // packed pairs: acc[i2][j] = (query i = 2 i2, query i = 2 i2 + 1) x
 // candidate j, i.e. query rows qbase + 8 i2 and qbase + 8 i2 + 4, candidate
 // row pbase + 8 j.  The query tile Q2 stores those two rows interleaved
-// (pair row pid = 16 wq + lq + 4 i2), so one 16-byte load gives both queries'
+// (pair row pid = pidbase + 4 i2), so one 16-byte load gives both queries'
 // dimensions k and k+1.
 template <int MQ, int MP>
 __device__ __forceinline__ float acc_at(const f32x2 (&acc)[MQ / 2][MP], int i, int j)
@@ -150,27 +235,40 @@ __device__ __forceinline__ float block_min(const f32x2 (&acc)[MQ / 2][MP])
 
 // Resident blocks per SM the register budget is sized for.
 #ifndef HISS_REFINE_MINB
-#define HISS_REFINE_MINB 2
+#define HISS_REFINE_MINB 3
 #endif
 
+
+// One thread block refines one unit: a tile of up to TQ queries of one grid
+// cell against one chunk of up to kCH candidates of the cell's concatenated
+// stencil.  The producer warp streams the chunk through a ring of staged
+// candidate tiles (cp.async per 16-byte chunk, completion tracked by the
+// stage's "full" mbarrier); each compute warp waits for a stage, refines its
+// 4 MQ x 32 block of pairs with early termination, writes its mask words and
+// releases the stage on its "empty" mbarrier.  Warps never wait for one
+// another within a tile, so a warp whose pairs all leave after 4 dimensions
+// moves on to the next tile while others finish.
+//
 // PROF = true: no mask output; instead count, over all candidate pairs, the
 // dimensions a pair needs when it stops at the first multiple of 4 whose
 // partial sum exceeds eps^2 (prof[0]), and the dimensions the warp-level
 // schedule of the PROF = false kernel executes (prof[1]).
 template <int MQ, int MP, bool PROF>
-__global__ void __launch_bounds__(kThreads, HISS_REFINE_MINB) k_refine(const RefineArgs a)
+__global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(const RefineArgs a)
 {
-    using T = Tile<MQ, MP>;
-    extern __shared__ __align__(16) float smem[];
+    constexpr int kTQ = Geo<MQ, MP>::TQ, kTP = Geo<MQ, MP>::TP;
+    extern __shared__ __align__(128) float smem[];
+    __shared__ __align__(8) uint64_t s_full[kMaxStages];
+    __shared__ __align__(8) uint64_t s_empty[kMaxStages];
     __shared__ int32_t s_nstart[kStencil];
     __shared__ int32_t s_vpre[kStencil + 1];
     __shared__ int64_t s_info[2];
-    __shared__ int32_t s_src[2][T::TP];  // source row of each candidate row of a staged tile (-1: none)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d4 = a.d4, S = tile_stride(d4), S2 = pair_stride(d4), C4 = d4 / 4;
+    const int nst = refine_stages<MQ, MP>(d4);
     float *Q2 = smem;
-    float *Ps0 = smem + (T::TQ / 2) * S2;
+    float *P0 = smem + (kTQ / 2) * S2;
 
     if (tid == 0) {
         const int64_t u = a.unit0 + blockIdx.x;
@@ -181,6 +279,11 @@ __global__ void __launch_bounds__(kThreads, HISS_REFINE_MINB) k_refine(const Ref
         }
         s_info[0] = lo;
         s_info[1] = u - a.tile_unit[lo];
+        for (int st = 0; st < nst; ++st) {
+            mbar_init(&s_full[st], 32);
+            mbar_init(&s_empty[st], kComputeWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
     const int64_t t = s_info[0];
@@ -191,8 +294,8 @@ __global__ void __launch_bounds__(kThreads, HISS_REFINE_MINB) k_refine(const Ref
     const int64_t B = a.bound[c];
     const int64_t W = (B + 31) >> 5;           // meaningful words of a mask row
     const int64_t W4 = (W + 3) & ~int64_t(3);  // row stride (16-byte rows)
-    const int ns = a.nbr_cnt[c];
-    if (tid < ns) {
+    const int ncell = a.nbr_cnt[c];
+    if (tid < ncell) {
         const int32_t nb = a.nbr[(int64_t)c * kStencil + tid];
         s_nstart[tid] = a.cell_start[nb];
         s_vpre[tid + 1] = a.cell_start[nb + 1] - a.cell_start[nb];
@@ -200,12 +303,57 @@ __global__ void __launch_bounds__(kThreads, HISS_REFINE_MINB) k_refine(const Ref
     __syncthreads();
     if (tid == 0) {
         s_vpre[0] = 0;
-        for (int i = 1; i <= ns; ++i) s_vpre[i] += s_vpre[i - 1];
+        for (int i = 1; i <= ncell; ++i) s_vpre[i] += s_vpre[i - 1];
+    }
+    __syncthreads();
+
+    const int64_t vbeg = chunk * kCH;
+    const int64_t vend = min(B, vbeg + (int64_t)kCH);
+    const int ntiles = (int)((vend - vbeg + kTP - 1) / kTP);
+
+    if (warp == kComputeWarps) {
+        // ---- producer warp: stream the chunk through the stage ring ----
+        // Each lane copies the 16-byte chunks of rows lane and lane + 32 of
+        // a staged tile (cp.async), then arrives on the stage's full barrier
+        // twice: once asynchronously when its copies land, once now.
+        for (int it = 0; it < ntiles; ++it) {
+            const int st = it % nst;
+            const uint32_t round = (uint32_t)(it / nst);
+            if (it >= nst && !mbar_wait(&s_empty[st], (round - 1u) & 1u)) {
+                atomicExch(&a.flags[kFlagRefineTimeout], 1);
+                return;
+            }
+            float *P = P0 + st * kTP * S;
+            const int64_t v0 = vbeg + (int64_t)it * kTP;
+#pragma unroll
+            for (int h = 0; h < kTP / 32; ++h) {
+                const int r = lane + 32 * h;
+                const int64_t v = v0 + r;
+                float4 *row = reinterpret_cast<float4 *>(P + r * S);
+                if (v < vend) {
+                    int lo = 0, hi = ncell - 1;  // last slot with s_vpre[slot] <= v
+                    while (lo < hi) {
+                        const int mid = (lo + hi + 1) >> 1;
+                        if (s_vpre[mid] <= v) lo = mid; else hi = mid - 1;
+                    }
+                    const float *src = a.xs + (int64_t)(s_nstart[lo] + (int32_t)(v - s_vpre[lo])) * d4;
+                    for (int cc = 0; cc < C4; ++cc) cp_async16(row + cc, src + 4 * cc);
+                } else {
+                    // no candidate: -inf makes every distance to this row +inf
+                    for (int cc = 0; cc < C4; ++cc)
+                        row[cc] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                }
+            }
+            cp_async_arrive_on(&s_full[st]);
+            mbar_arrive(&s_full[st]);
+        }
+        return;
     }
 
+    // ---- compute warps ----
     // query tile, pair-interleaved: pair row pid holds rows a = 8 (pid / 4) +
     // pid % 4 and a + 4, dimension by dimension; rows >= nq are +inf
-    for (int idx = tid; idx < (T::TQ / 2) * C4; idx += kThreads) {
+    for (int idx = tid; idx < (kTQ / 2) * C4; idx += kComputeThreads) {
         const int pid = idx / C4, cc = idx - pid * C4;
         const int ra = 8 * (pid >> 2) + (pid & 3), rb = ra + 4;
         const float4 inf4 = make_float4(INFINITY, INFINITY, INFINITY, INFINITY);
@@ -215,98 +363,47 @@ __global__ void __launch_bounds__(kThreads, HISS_REFINE_MINB) k_refine(const Ref
         dst[0] = make_float4(x.x, y.x, x.y, y.y);
         dst[1] = make_float4(x.z, y.z, x.w, y.w);
     }
-    __syncthreads();  // s_vpre complete
-
-    const int64_t vbeg = chunk * T::CH;
-    const int64_t vend = min(B, vbeg + (int64_t)T::CH);
-    const int ntiles = (int)((vend - vbeg + T::TP - 1) / T::TP);
-
-    // source rows of candidate tile v0 .. v0 + TP, looked up once per row
-    auto fill_src = [&](int buf, int64_t v0) {
-        for (int r = tid; r < T::TP; r += kThreads) {
-            const int64_t v = v0 + r;
-            int32_t src = -1;
-            if (v < vend) {
-                int lo = 0, hi = ns - 1;  // last slot with s_vpre[slot] <= v
-                while (lo < hi) {
-                    const int mid = (lo + hi + 1) >> 1;
-                    if (s_vpre[mid] <= v) lo = mid; else hi = mid - 1;
-                }
-                src = s_nstart[lo] + (int32_t)(v - s_vpre[lo]);
-            }
-            s_src[buf][r] = src;
-        }
-    };
-    // this thread's first (row, 16-byte chunk) of a staged tile and the step
-    const int r_first = tid / C4, c_first = tid - (tid / C4) * C4;
-    const int r_step = kThreads / C4, c_step = kThreads - (kThreads / C4) * C4;
-    auto load_p = [&](int buf) {
-        float *P = Ps0 + buf * T::TP * S;
-        int r = r_first, cc = c_first;
-        for (int idx = tid; idx < T::TP * C4; idx += kThreads) {
-            float *dst = P + r * S + 4 * cc;
-            const int32_t src = s_src[buf][r];
-            if (src >= 0) cp_async16(dst, a.xs + (int64_t)src * d4 + 4 * cc);
-            else *reinterpret_cast<float4 *>(dst) = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-            r += r_step;
-            cc += c_step;
-            if (cc >= C4) {
-                cc -= C4;
-                ++r;
-            }
-        }
-    };
-
-    fill_src(0, vbeg);
-    if (ntiles > 1) fill_src(1, vbeg + T::TP);
-    __syncthreads();
-    load_p(0);
-    cp_async_commit();
+    compute_warps_sync();
 
     const int wq = warp >> 1, wp = warp & 1;
     const int lq = lane >> 3, lp = lane & 7;
-    const int qbase = wq * (4 * MQ) + lq;  // query row i: qbase + 4 i
-    const int pidbase = wq * (2 * MQ) + lq; // pair row of queries 2 i2, 2 i2 + 1: pidbase + 4 i2
-    const int pbase = wp * (8 * MP) + lp;  // candidate row j: pbase + 8 j
+    const int qbase = wq * (4 * MQ) + lq;    // query row i: qbase + 4 i
+    const int pidbase = wq * (2 * MQ) + lq;  // pair row of queries 2 i2, 2 i2 + 1: pidbase + 4 i2
+    const int pbase = wp * (8 * MP) + lp;    // candidate row j: pbase + 8 j
     const float eps2 = a.eps2;
-    uint32_t my_count = 0;                 // neighbours of query row qbase + 4 lp (lp < MQ)
+    uint32_t my_count = 0;                   // neighbours of query row qbase + 4 lp (lp < MQ)
     const int64_t row_word0 = a.tile_word[t] - a.word0;
     uint64_t prof_alg = 0, prof_exec = 0;
 
     for (int it = 0; it < ntiles; ++it) {
-        const int64_t v0 = vbeg + (int64_t)it * T::TP;
-        if (it + 1 < ntiles) {
-            load_p((it + 1) & 1);
-            cp_async_commit();
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
+        const int st = it % nst;
+        const uint32_t round = (uint32_t)(it / nst);
+        if (!mbar_wait(&s_full[st], round & 1u)) {
+            atomicExch(&a.flags[kFlagRefineTimeout], 1);
+            return;
         }
-        __syncthreads();
-
-        const float *P = Ps0 + (it & 1) * T::TP * S;
+        const int64_t v0 = vbeg + (int64_t)it * kTP;
+        const float *P = P0 + st * kTP * S;
         f32x2 acc[MQ / 2][MP];
         if constexpr (PROF) {
             // all dimensions, counting live pairs step by step
             bool warp_live = true;
             block_step2<MQ, MP, true>(acc, Q2, P, S2, S, pidbase, pbase, 0);
             block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, 2);
-            int live = 0;
+            int valid = 0;
 #pragma unroll
             for (int i = 0; i < MQ; ++i)
 #pragma unroll
-                for (int j = 0; j < MP; ++j) live += (qbase + 4 * i < nq && v0 + pbase + 8 * j < vend) ? 1 : 0;
-            const int valid = live;
+                for (int j = 0; j < MP; ++j) valid += (qbase + 4 * i < nq && v0 + pbase + 8 * j < vend) ? 1 : 0;
             prof_alg += (uint64_t)valid * (uint64_t)min(4, a.d);
             prof_exec += (uint64_t)valid * (uint64_t)min(4, a.d);
             for (int k = 4; k < d4; k += 4) {
-                live = 0;
+                int live = 0;
 #pragma unroll
                 for (int i = 0; i < MQ; ++i)
 #pragma unroll
                     for (int j = 0; j < MP; ++j) live += (acc_at<MQ, MP>(acc, i, j) <= eps2) ? 1 : 0;
-                if (k < 16 || (k & 7) == 0)
-                    if (__all_sync(0xffffffffu, block_min<MQ, MP>(acc) > eps2)) warp_live = false;
+                if (__all_sync(0xffffffffu, block_min<MQ, MP>(acc) > eps2)) warp_live = false;
                 if (!__any_sync(0xffffffffu, live > 0) && !warp_live) break;
                 const uint64_t step = (uint64_t)min(4, a.d - k);
                 prof_alg += (uint64_t)live * step;
@@ -314,64 +411,55 @@ __global__ void __launch_bounds__(kThreads, HISS_REFINE_MINB) k_refine(const Ref
                 block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k);
                 block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k + 2);
             }
-            if (it + 2 < ntiles) fill_src(it & 1, v0 + 2 * T::TP);
-            __syncthreads();
-            continue;
-        }
-        block_step2<MQ, MP, true>(acc, Q2, P, S2, S, pidbase, pbase, 0);
-        block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, 2);
-        // warp-level early termination: checked after 4, 8 and 12 dimensions,
-        // then every 8 (the pairs are in variance order, most leave early)
-        bool any_close = true;
-        for (int k = 4;; k += 4) {
-            if (k == d4) {
-                any_close = __any_sync(0xffffffffu, block_min<MQ, MP>(acc) <= eps2);
-                break;
-            }
-            if (k < 16 || (k & 7) == 0) {
+        } else {
+            block_step2<MQ, MP, true>(acc, Q2, P, S2, S, pidbase, pbase, 0);
+            block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, 2);
+            // warp-level early termination (the pairs are in variance order,
+            // most leave early)
+            bool any_close = true;
+            for (int k = 4;; k += 4) {
+                if (k == d4) {
+                    any_close = __any_sync(0xffffffffu, block_min<MQ, MP>(acc) <= eps2);
+                    break;
+                }
                 if (__all_sync(0xffffffffu, block_min<MQ, MP>(acc) > eps2)) {
                     any_close = false;
                     break;
                 }
+                block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k);
+                block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k + 2);
             }
-            block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k);
-            block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k + 2);
-        }
-
-        // one bit per pair; OR across the 8 lanes of a query row; lane lp
-        // writes the words of query j = lp
-        const int64_t word_tile = v0 >> 5;
-        if (any_close) {
+            // one bit per pair.  The warp's 32 candidate columns (pbase + 8 j)
+            // form one mask word per query row: bit lp + 8 j.  A ballot per
+            // (i, j) gives, for each lq, byte lq = the 8 lanes' bits; three
+            // byte permutes assemble the word of query row qbase + 4 i.  Lane
+            // lp keeps the word of i = lp and writes it.
+            static_assert(MP == 4, "one mask word per query row per warp");
+            const int64_t wcol = (v0 >> 5) + wp;
+            const int qr = qbase + 4 * lp;
+            if (any_close) {
+                const uint32_t sel = (uint32_t)lq | ((uint32_t)(lq + 4) << 4);
+                uint32_t mine = 0;
 #pragma unroll
-            for (int i = 0; i < MQ; ++i) {
+                for (int i = 0; i < MQ; ++i) {
+                    uint32_t bj[MP];
 #pragma unroll
-                for (int wi = 0; wi < T::WPW; ++wi) {
-                    uint32_t w = 0;
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj)
-                        w |= (acc_at<MQ, MP>(acc, i, 4 * wi + jj) <= eps2 ? 1u : 0u) << (lp + 8 * jj);
-                    w |= __shfl_xor_sync(0xffffffffu, w, 1);
-                    w |= __shfl_xor_sync(0xffffffffu, w, 2);
-                    w |= __shfl_xor_sync(0xffffffffu, w, 4);
-                    const int qr = qbase + 4 * i;
-                    const int64_t wcol = word_tile + wp * T::WPW + wi;
-                    if (lp == i && qr < nq && wcol < W) {
-                        a.mask[row_word0 + (int64_t)qr * W4 + wcol] = w;
-                        my_count += __popc(w);
-                    }
+                    for (int j = 0; j < MP; ++j) bj[j] = __ballot_sync(0xffffffffu, acc_at<MQ, MP>(acc, i, j) <= eps2);
+                    const uint32_t w01 = __byte_perm(bj[0], bj[1], sel), w23 = __byte_perm(bj[2], bj[3], sel);
+                    const uint32_t w = __byte_perm(w01, w23, 0x5410);
+                    if (lp == i) mine = w;
                 }
-            }
-        } else if (lp < MQ && qbase + 4 * lp < nq) {
-            // no pair of the warp is within eps: zero words for this lane's row
-            uint32_t *row = a.mask + row_word0 + (int64_t)(qbase + 4 * lp) * W4;
-#pragma unroll
-            for (int wi = 0; wi < T::WPW; ++wi) {
-                const int64_t wcol = word_tile + wp * T::WPW + wi;
-                if (wcol < W) row[wcol] = 0u;
+                if (lp < MQ && qr < nq && wcol < W) {
+                    a.mask[row_word0 + (int64_t)qr * W4 + wcol] = mine;
+                    my_count += __popc(mine);
+                }
+            } else if (lp < MQ && qr < nq && wcol < W) {
+                // no pair of the warp is within eps: a zero word for this lane's row
+                a.mask[row_word0 + (int64_t)qr * W4 + wcol] = 0u;
             }
         }
-        if (it + 2 < ntiles) fill_src(it & 1, v0 + 2 * T::TP);
-        __syncthreads();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_empty[st]);
     }
     if constexpr (PROF) {
 #pragma unroll
@@ -394,16 +482,14 @@ __global__ void __launch_bounds__(kThreads, HISS_REFINE_MINB) k_refine(const Ref
 template <int MQ, int MP, bool PROF>
 cudaError_t launch_refine(const RefineArgs &a, cudaStream_t s)
 {
-    using T = Tile<MQ, MP>;
-    const size_t smem = sizeof(float) * ((size_t)(T::TQ / 2) * pair_stride(a.d4) + (size_t)2 * T::TP * tile_stride(a.d4));
+    const size_t smem = refine_smem<MQ, MP>(a.d4);
     static size_t configured = 0;  // largest dynamic shared memory requested so far
     if (smem > configured) {
-        HISS_TRY(cudaFuncSetAttribute(k_refine<MQ, MP, PROF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)smem));
+        HISS_TRY(cudaFuncSetAttribute(k_refine<MQ, MP, PROF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
         configured = smem;
     }
     if (a.nunits <= 0) return cudaSuccess;
-    k_refine<MQ, MP, PROF><<<(unsigned)a.nunits, kThreads, smem, s>>>(a);
+    k_refine<MQ, MP, PROF><<<(unsigned)a.nunits, kRefineThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -528,23 +614,21 @@ __global__ void k_word_positions(const uint32_t *words, int64_t nbits, const int
 
 }  // namespace
 
-int refine_tq(int d4) { return d4 <= 128 ? Tile<8, 8>::TQ : Tile<4, 4>::TQ; }
+int refine_tq(int d4) { return d4 <= 64 ? Geo<8, 4>::TQ : Geo<4, 4>::TQ; }
 
 cudaError_t refine(const RefineArgs &a, cudaStream_t s, int64_t *launches)
 {
     ++*launches;
-    if (a.d4 <= 128) return launch_refine<8, 8, false>(a, s);
-    return launch_refine<4, 4, false>(a, s);
+    return a.d4 <= 64 ? launch_refine<8, 4, false>(a, s) : launch_refine<4, 4, false>(a, s);
 }
 
 cudaError_t refine_profile(const RefineArgs &a, cudaStream_t s, int64_t *launches)
 {
     ++*launches;
-    if (a.d4 <= 128) return launch_refine<8, 8, true>(a, s);
-    return launch_refine<4, 4, true>(a, s);
+    return a.d4 <= 64 ? launch_refine<8, 4, true>(a, s) : launch_refine<4, 4, true>(a, s);
 }
 
-int refine_chunk(int d4) { return d4 <= 128 ? Tile<8, 8>::CH : Tile<4, 4>::CH; }
+int refine_chunk(int) { return kCH; }
 
 cudaError_t compact(const CompactArgs &a, cudaStream_t s, int64_t *launches)
 {
