@@ -100,11 +100,13 @@ hiss_join_queries = _sig("hiss_join_queries", ctypes.c_int,
                          [_p, _p, _i64, _f32, ctypes.c_size_t, ctypes.POINTER(hiss_out)])
 hiss_count_queries = _sig("hiss_count_queries", ctypes.c_int, [_p, _p, _i64, _f32, _p])
 hiss_exclusive_scan_noalloc = _sig("hiss_exclusive_scan_noalloc", ctypes.c_int, [_p, _p, _p, _i64])
+hiss_gram_tf32 = _sig("hiss_gram_tf32", ctypes.c_int, [_p, _p, _p, _i32, _p])
 
 EXPORTED = ["hiss_create", "hiss_destroy", "hiss_build", "hiss_build_host", "hiss_count", "hiss_join",
             "hiss_index", "hiss_last_stats", "hiss_launch_count", "hiss_strerror", "hiss_last_cuda_error",
             "hiss_set_option", "hiss_sort_pairs", "hiss_exclusive_scan", "hiss_mask_positions",
-            "hiss_exclusive_scan_noalloc", "hiss_work_profile", "hiss_join_queries", "hiss_count_queries"]
+            "hiss_exclusive_scan_noalloc", "hiss_work_profile", "hiss_join_queries", "hiss_count_queries",
+            "hiss_gram_tf32"]
 
 
 class HissError(RuntimeError):

@@ -1053,4 +1053,15 @@ int hiss_mask_positions(hiss_ctx *ctx, const uint32_t *d_words, int64_t nbits, i
     return sync(ctx);
 }
 
+int hiss_gram_tf32(hiss_ctx *ctx, const float *d_a, const float *d_b, int32_t k, float *d_out)
+{
+    ST(enter(ctx));
+    if (!d_a || !d_b || !d_out || k < 8 || k > 128 || k % 8 != 0) return HISS_E_ARG;
+    ST(ensure(ctx, ctx->flags, sizeof(int) * kNumFlags * 2));
+    CK(cudaMemsetAsync(ctx->flags.p, 0, sizeof(int) * kNumFlags, ctx->stream));
+    CK(gram_tf32(d_a, d_b, k, d_out, as<int>(ctx->flags), ctx->stream, &ctx->launches));
+    ST(sync(ctx));
+    return check_flags(ctx);
+}
+
 }  // extern "C"

@@ -145,4 +145,9 @@ cudaError_t compact(const CompactArgs &a, cudaStream_t s, int64_t *launches);
 cudaError_t mask_positions(const uint32_t *words, int64_t nbits, int64_t *pos, int64_t *count,
                            int64_t *tmp, cudaStream_t s, int64_t *launches);
 
+// ---- tensor cores (refine_tc.cu) ----------------------------------------------
+// G = tf32(a) tf32(b)^T for two 128 x k float32 blocks (k % 8 == 0, k <= 128).
+cudaError_t gram_tf32(const float *a, const float *b, int k, float *out, int *flags, cudaStream_t s,
+                      int64_t *launches);
+
 }  // namespace hiss

@@ -17,6 +17,7 @@
 // written to the query's mask row; the popcount of each word is accumulated
 // into the query's neighbour count.
 #include "hiss_internal.cuh"
+#include "ptx.cuh"
 
 namespace hiss {
 namespace {
@@ -49,7 +50,6 @@ struct Geo {
     static constexpr int TP = kCandWarps * 8 * MP;   // candidates per staged tile
 };
 constexpr int kMaxStages = 4;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a stage wait gives up after 2 s
 
 // Stages of the candidate ring: as many as fit (up to 4, at least 2) in
 // about a third of the SM's shared memory, so that two or three blocks stay
@@ -113,63 +113,6 @@ __device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c)
     return r;
 }
 
-// ---- mbarrier and asynchronous-copy primitives (inline PTX) ---------------------
-__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
-{
-    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
-{
-    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
-                     smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok)
-                 : "r"(smem_u32(bar)), "r"(parity)
-                 : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ uint64_t global_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-// Wait for the phase of the given parity to complete.  Gives up (returns
-// false) after kWaitLimitNs, so a logic error can never hang the GPU.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
-{
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
-    }
-}
-// 16-byte asynchronous copy global -> shared (L1 bypass).
-__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
-}
-// Make the mbarrier track completion of all cp.async issued so far by this
-// thread: the pending count is raised now and lowered when they complete.
-__device__ __forceinline__ void cp_async_arrive_on(uint64_t *bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 __device__ __forceinline__ void compute_warps_sync()
 {
     asm volatile("bar.sync 1, %0;" ::"n"(kComputeThreads) : "memory");

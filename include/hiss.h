@@ -253,6 +253,16 @@ int hiss_exclusive_scan(hiss_ctx *ctx, const int64_t *d_in, int64_t *d_out, int6
  * number to *h_count (host).  d_pos must hold nbits entries. */
 int hiss_mask_positions(hiss_ctx *ctx, const uint32_t *d_words, int64_t nbits, int64_t *d_pos, int64_t *h_count);
 
+/* Gram matrix on the tensor cores: out[i][j] = sum_k tf32(a[i][k]) *
+ * tf32(b[j][k]) for two 128 x k float32 row-major device blocks (k a
+ * multiple of 8, 8 <= k <= 128), out a device float32[128][128].  tf32(x)
+ * rounds to 10 explicit mantissa bits, to nearest with ties away from zero;
+ * the products are exact in float32 and the sums are accumulated in float32
+ * by tcgen05.mma (kind::tf32).  This is the inner product that the
+ * tensor-core refinement evaluates (see HISS_OPT_REFINE); exposed to test the
+ * tensor-core operand layout. */
+int hiss_gram_tf32(hiss_ctx *ctx, const float *d_a, const float *d_b, int32_t k, float *d_out);
+
 /* ---- allocation-free variant ---------------------------------------------
  * The paper has no counterpart to this entry point; it exists for callers
  * that cannot allocate device memory (a plugin inside a host framework that

@@ -79,3 +79,36 @@ def test_compaction_random_masks(ctx, nbits):
     pos = torch.empty(nbits, dtype=torch.int64, device="cuda")
     cnt = ctx.mask_positions(words_t, nbits, pos)
     assert np.array_equal(pos[:cnt].cpu().numpy(), oracle.compact_mask(bits))
+
+
+def _tf32_rna(x):
+    """float32 -> TF32 (10 explicit mantissa bits), to nearest, ties away
+    from zero, done on the bit pattern (test-side restatement of the
+    rounding that the tensor-core operands get)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    r = ((u + np.uint32(0x1000)) & np.uint32(0xFFFFE000)).astype(np.uint32)
+    return r.view(np.float32)
+
+
+@pytest.mark.parametrize("k", [8, 16, 40, 72, 128])
+def test_gram_tf32_on_tensor_cores(ctx, k):
+    import ctypes
+    import exact_dimensional_distance_gb300 as edd
+    rng = np.random.default_rng(500 + k)
+    a = (rng.standard_normal((128, k)) * rng.uniform(0.1, 10, size=(128, 1))).astype(np.float32)
+    b = (rng.standard_normal((128, k)) * rng.uniform(0.1, 10, size=(128, 1))).astype(np.float32)
+    a[5, :] = 0.0          # an all-zero row
+    b[:, 3] = 1.0          # a constant column
+    at, bt = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    out = torch.full((128, 128), float("nan"), dtype=torch.float32, device="cuda")
+    rc = edd.hiss_gram_tf32(ctx._h, ctypes.c_void_p(at.data_ptr()), ctypes.c_void_p(bt.data_ptr()), k,
+                            ctypes.c_void_p(out.data_ptr()))
+    assert rc == edd.HISS_OK, edd.hiss_strerror(rc)
+    ta, tb = _tf32_rna(a).astype(np.float64), _tf32_rna(b).astype(np.float64)
+    want = ta @ tb.T
+    # float32 accumulation of k exact products: error <= k 2^-22 sum |a_k b_k|
+    bound = (k + 8) * 2.0 ** -22 * (np.abs(ta) @ np.abs(tb).T) + 1e-30
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - want) <= bound), float(np.max(np.abs(got - want) / bound))
+    # TF32 rounding really happened (operands are not used at float32 precision)
+    assert not np.allclose(ta, a.astype(np.float64), rtol=0, atol=0)
