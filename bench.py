@@ -198,7 +198,9 @@ def workload_config(args, eps):
         name, n = name + " (reduced instance for profiling)", args.n
     return {"workload": "%s N=%d d=%d mean_neighbours=%d" % (name, n, d, k), "n": n, "d": d, "eps": eps,
             "eps_hex": float(eps).hex(), "batch_bytes": args.batch_bytes, "l2": "flushed between steps",
-            "parallelism": "replica per GPU"}
+            "parallelism": "replica per GPU",
+            "refine": "tensor cores (TF32 Gram prefilter + exact recheck)" if getattr(args, "refine", "cuda") == "tensor"
+            else "CUDA cores"}
 
 
 def cpu_baseline(args, x, eps):
@@ -222,6 +224,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", type=int, default=2)
     ap.add_argument("--impl", default="hiss", choices=["hiss", "reference"])
+    ap.add_argument("--refine", default="cuda", choices=["cuda", "tensor"],
+                    help="refinement: CUDA cores (default) or the tensor-core prefilter with exact recheck")
     ap.add_argument("--batch-bytes", type=int, default=32 << 30)
     ap.add_argument("--ref-rows", type=int, default=8000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -254,6 +258,7 @@ def main():
     with torch.cuda.stream(stream):
         xd = torch.from_numpy(x).cuda()
         j = edd.Join(stream)
+        j.set_refine(args.refine == "tensor")
     torch.cuda.synchronize()
 
     def step():

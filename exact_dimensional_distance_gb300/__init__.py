@@ -38,6 +38,9 @@ HISS_E_CALLBACK = -7
 HISS_OUT_CSR = 0
 HISS_OUT_MASK = 1
 HISS_OPT_ALLOC_LIMIT = 1
+HISS_OPT_REFINE = 2
+HISS_REFINE_CUDA_CORES = 0
+HISS_REFINE_TENSOR_CORES = 1
 HISS_MAX_DIM = 256
 
 _i64, _i32, _f32, _p = ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p
@@ -334,6 +337,13 @@ class Join:
 
     def set_alloc_limit(self, nbytes):
         _check(hiss_set_option(self._h, HISS_OPT_ALLOC_LIMIT, int(nbytes)), self._h, "hiss_set_option")
+
+    def set_refine(self, tensor_cores):
+        """Select the refinement: CUDA cores (default) or the tensor-core
+        prefilter with exact recheck (HISS_OPT_REFINE)."""
+        mode = HISS_REFINE_TENSOR_CORES if tensor_cores else HISS_REFINE_CUDA_CORES
+        _check(hiss_set_option(self._h, HISS_OPT_REFINE, mode), self._h, "hiss_set_option")
+        return self
 
     # building blocks
     def sort_pairs(self, keys, vals, key_bits):

@@ -56,6 +56,8 @@ struct hiss_ctx {
 
     // query tiles in processing order
     bool tiles_valid = false;
+    int tiles_tc = 0;           // the cached tiles were cut for the tensor-core refinement
+    int refine_mode = HISS_REFINE_CUDA_CORES;
     int64_t T = 0, total_units = 0, total_words = 0;
     DBuf lpt_keys, lpt_order, ntiles, tile_off, tile_cell, tile_q0, tile_nq, tile_word, tile_unit, tile_qoff;
     uint32_t *order = nullptr;
@@ -388,12 +390,20 @@ QuerySide self_side(hiss_ctx *ctx)
     return q;
 }
 
+// The refinement a join runs: the tensor-core one when selected and the
+// dimension fits it, else the CUDA-core one.
+bool use_tc(const hiss_ctx *ctx)
+{
+    return ctx->refine_mode == HISS_REFINE_TENSOR_CORES && ctx->d4 <= refine_tc_max_d4();
+}
+
 // ---- query tiles in processing order (largest work first) ------------------------
-int build_tiles(hiss_ctx *ctx, const QuerySide &qs)
+int build_tiles(hiss_ctx *ctx, const QuerySide &qs, bool tc)
 {
     cudaStream_t s = ctx->stream;
     const int64_t C = qs.C;
-    const int tq = refine_tq(ctx->d4), chunk = refine_chunk(ctx->d4);
+    const int tq = tc ? refine_tc_tq() : refine_tq(ctx->d4);
+    const int chunk = tc ? refine_tc_chunk() : refine_chunk(ctx->d4);
     ST(ensure(ctx, ctx->lpt_keys, 8 * (size_t)C));
     ST(ensure(ctx, ctx->lpt_order, 4 * (size_t)C));
     ST(ensure(ctx, ctx->ntiles, 4 * (size_t)C));
@@ -451,11 +461,13 @@ int build_tiles(hiss_ctx *ctx, const QuerySide &qs)
 }
 
 // Tiles of the self-join, cached with the index.
-int ensure_tiles(hiss_ctx *ctx)
+int ensure_tiles(hiss_ctx *ctx, bool tc)
 {
-    if (ctx->tiles_valid) return HISS_OK;
-    ST(build_tiles(ctx, self_side(ctx)));
+    if (ctx->tiles_valid && ctx->tiles_tc == (int)tc) return HISS_OK;
+    ctx->tiles_valid = false;
+    ST(build_tiles(ctx, self_side(ctx), tc));
     ctx->tiles_valid = true;
+    ctx->tiles_tc = (int)tc;
     return HISS_OK;
 }
 
@@ -483,6 +495,7 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
 {
     const int mode = out ? out->mode : HISS_OUT_CSR;
     const int to_host = out ? out->copy_to_host : 0;
+    const bool tc = use_tc(ctx);  // the tiles were cut for this refinement
     hiss_batch_fn fn = out ? out->on_batch : nullptr;
     void *user = out ? out->user : nullptr;
     cudaStream_t s = ctx->stream;
@@ -560,7 +573,8 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
         ra.prof = nullptr;
         ra.flags = as<int>(ctx->flags);
         CK(cudaEventRecord(ctx->ev[4], s));
-        CK(refine(ra, s, &ctx->launches));
+        if (tc) CK(refine_tc(ra, eps, s, &ctx->launches));
+        else CK(refine(ra, s, &ctx->launches));
         CK(cudaEventRecord(ctx->ev[5], s));
 
         CompactArgs ca{};
@@ -676,7 +690,7 @@ int do_join(hiss_ctx *ctx, float eps, size_t batch_bytes, const hiss_out *out)
         ms_index = ctx->st.ms_index;
     }
     CK(cudaEventRecord(ctx->ev[2], s));
-    ST(ensure_tiles(ctx));
+    ST(ensure_tiles(ctx, use_tc(ctx)));
     CK(cudaEventRecord(ctx->ev[3], s));
     fill_grid_stats(ctx);
     return run_batches(ctx, self_side(ctx), eps, batch_bytes, out, ms_index, launches0);
@@ -787,7 +801,7 @@ int do_semi(hiss_ctx *ctx, const float *d_queries, int64_t nq, float eps, size_t
         return HISS_OK;
     }
     ctx->tiles_valid = false;  // the tile arrays now describe the queries
-    ST(build_tiles(ctx, qs));
+    ST(build_tiles(ctx, qs, use_tc(ctx)));
     CK(cudaEventRecord(ctx->ev[3], s));
     return run_batches(ctx, qs, eps, batch_bytes, out, ms_index, launches0);
 }
@@ -919,7 +933,7 @@ int hiss_work_profile(hiss_ctx *ctx, float eps, int64_t *out)
     if (!ctx->built) return HISS_E_STATE;
     if (!(eps >= 0.0f) || std::isinf(eps)) return HISS_E_ARG;
     ST(ensure_grid(ctx, eps));
-    ST(ensure_tiles(ctx));
+    ST(ensure_tiles(ctx, false));  // the work counter is the CUDA-core kernel's
     ST(ensure(ctx, ctx->nb_d, 64));
     CK(cudaMemsetAsync(ctx->nb_d.p, 0, 16, ctx->stream));
     RefineArgs ra{};
@@ -1006,6 +1020,11 @@ int hiss_set_option(hiss_ctx *ctx, int option, int64_t value)
     if (option == HISS_OPT_ALLOC_LIMIT) {
         if (value < 0) return HISS_E_ARG;
         ctx->alloc_limit = value;
+        return HISS_OK;
+    }
+    if (option == HISS_OPT_REFINE) {
+        if (value != HISS_REFINE_CUDA_CORES && value != HISS_REFINE_TENSOR_CORES) return HISS_E_ARG;
+        ctx->refine_mode = (int)value;
         return HISS_OK;
     }
     return HISS_E_ARG;

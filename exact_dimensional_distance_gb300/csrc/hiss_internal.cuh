@@ -146,6 +146,14 @@ cudaError_t mask_positions(const uint32_t *words, int64_t nbits, int64_t *pos, i
                            int64_t *tmp, cudaStream_t s, int64_t *launches);
 
 // ---- tensor cores (refine_tc.cu) ----------------------------------------------
+// Refinement of a batch with the squared distances from TF32 Gram matrices on
+// the tensor cores and an exact float32 recheck of every undecided pair;
+// same units, tiles (refine_tc_tq() queries, refine_tc_chunk() candidates
+// per unit) and mask as refine().  d4 <= refine_tc_max_d4().
+int refine_tc_max_d4();
+int refine_tc_tq();
+int refine_tc_chunk();
+cudaError_t refine_tc(const RefineArgs &a, float eps, cudaStream_t s, int64_t *launches);
 // G = tf32(a) tf32(b)^T for two 128 x k float32 blocks (k % 8 == 0, k <= 128).
 cudaError_t gram_tf32(const float *a, const float *b, int k, float *out, int *flags, cudaStream_t s,
                       int64_t *launches);

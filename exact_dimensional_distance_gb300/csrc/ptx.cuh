@@ -48,12 +48,16 @@ __device__ __forceinline__ uint64_t global_ns()
 }
 // Wait for the phase of the given parity to complete.  Gives up (returns
 // false) after kWaitLimitNs, or as soon as *abort becomes non-zero (when
-// abort is given), so a logic error can never hang the GPU.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *abort = nullptr)
+// abort is given), so a logic error can never hang the GPU.  With sleep_ns >
+// 0 the waiting warp sleeps that long between polls, leaving the issue slots
+// to the warps it waits for.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const volatile int *abort = nullptr,
+                                          unsigned sleep_ns = 0)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
+        if (sleep_ns) __nanosleep(sleep_ns);
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0) {
             if (abort && *abort) return false;
@@ -68,6 +72,11 @@ __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src)
 {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
 }
+// Commit / wait for this thread's cp.async groups (N = groups that may stay pending).
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 // Make the mbarrier track completion of all cp.async issued so far by this
 // thread: the pending count is raised now and lowered when they complete.
 __device__ __forceinline__ void cp_async_arrive_on(uint64_t *bar)

@@ -217,8 +217,26 @@ const char *hiss_last_cuda_error(const hiss_ctx *ctx);
 /* Options.  HISS_OPT_ALLOC_LIMIT: cap, in bytes, on the device memory the
  * context may hold (0 = no cap); an allocation beyond it fails with
  * HISS_E_NOMEM without calling the CUDA allocator.  Used to test the
- * out-of-memory path without exhausting the device. */
-enum { HISS_OPT_ALLOC_LIMIT = 1 };
+ * out-of-memory path without exhausting the device.
+ *
+ * HISS_OPT_REFINE selects the refinement of hiss_join and hiss_join_queries:
+ *   HISS_REFINE_CUDA_CORES (default): float32 squared distances on the CUDA
+ *     cores, summed in variance order with early termination (RT-HiSS
+ *     Sections IV-A and IV-E);
+ *   HISS_REFINE_TENSOR_CORES: the same result mask from a prefilter on the
+ *     tensor cores (d <= 128; larger d uses the CUDA cores).  Per 128 x 128
+ *     tile of (query, candidate) pairs, the points are centred on the query
+ *     tile's mean and rounded to TF32, and the squared distance minus eps^2 is
+ *     obtained as a Gram matrix (tcgen05.mma) with the norms carried in extra
+ *     K columns.  A rigorous bound on the rounding and accumulation errors
+ *     decides most pairs from the sign; every pair inside the bound is
+ *     rechecked exactly (float32 sum in variance order).  Decided pairs agree
+ *     with the exact predicate dist <= eps; rechecked pairs are those of the
+ *     CUDA-core refinement.  No pages' counterpart: RT-HiSS refines on CUDA
+ *     cores only.
+ * Other options or values return HISS_E_ARG. */
+enum { HISS_OPT_ALLOC_LIMIT = 1, HISS_OPT_REFINE = 2 };
+enum { HISS_REFINE_CUDA_CORES = 0, HISS_REFINE_TENSOR_CORES = 1 };
 int hiss_set_option(hiss_ctx *ctx, int option, int64_t value);
 
 /* Work accounting for the refinement roofline (diagnostic; no result
