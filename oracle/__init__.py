@@ -422,3 +422,52 @@ def compact_mask(bits) -> np.ndarray:
     """Positions of the ones of a 0/1 result mask, in increasing order."""
     b = np.asarray(bits).astype(bool)
     return np.array([i for i in range(b.size) if b[i]], dtype=np.int64)
+
+
+# --------------------------------------------------------------------------
+# Exact k nearest neighbours (RT-HiSS Section VI, "exact kNN" built on the
+# epsilon join by growing eps)
+# --------------------------------------------------------------------------
+
+def knn(x, k: int, query_rows=None):
+    """The k nearest points of each query row, fp64 brute force.
+
+    Reading of the pages: RT-HiSS names exact kNN as a use of the epsilon
+    join (repeat the join with a growing eps for the queries that have fewer
+    than k neighbours, then keep the k nearest).  The result is the plain
+    definition: for query i, the k points j (the point itself included, at
+    distance 0) with the smallest squared distance s(i, j); equal distances
+    are ordered by the lower index.  Returns (ids int64 [q, k], dist2 float64
+    [q, k]), each row in increasing (s, j) order.
+    """
+    x = _points(x)
+    n = x.shape[0]
+    q = np.arange(n) if query_rows is None else np.asarray(query_rows, dtype=np.int64)
+    if not 1 <= k <= n:
+        raise ValueError("k must be in [1, n]")
+    x64 = x.astype(np.float64)
+    ids = np.empty((q.size, k), dtype=np.int64)
+    d2 = np.empty((q.size, k), dtype=np.float64)
+    for r, i in enumerate(q.tolist()):
+        s = ((x64 - x64[i]) ** 2).sum(axis=1)
+        order = np.lexsort((np.arange(n), s))[:k]  # by s, then by index
+        ids[r] = order
+        d2[r] = s[order]
+    return ids, d2
+
+
+def knn_py(x, k: int) -> list:
+    """Pure-Python kNN for tiny inputs (a second, independent restatement
+    used to pin ``knn``)."""
+    pts = [[float(v) for v in row] for row in _points(x)]
+    out = []
+    for i, a in enumerate(pts):
+        cand = []
+        for j, b in enumerate(pts):
+            s = 0.0
+            for u, v in zip(a, b):
+                s += (u - v) * (u - v)
+            cand.append((s, j))
+        cand.sort()
+        out.append([j for _, j in cand[:k]])
+    return out

@@ -246,3 +246,54 @@ def test_semi_join_matches_plain_loops_and_bound_covers():
     assert got == oracle.semi_brute_force_py(xq, xd, eps)
     bound = oracle.semi_count_bound(xq, xd, eps)
     assert all(bound[i] >= len(got[i]) for i in range(len(xq)))
+
+
+# ---- exact kNN oracle --------------------------------------------------------
+
+def test_knn_hand_case_1d_with_tie():
+    # points 0, 1, 3, 6, 10 on a line; k = 3, self first; point 2 (x = 3) is
+    # at 9 from both point 0 and point 3: the lower index wins
+    x = np.array([[0], [1], [3], [6], [10]], np.float32)
+    ids, d2 = oracle.knn(x, 3)
+    assert ids.tolist() == [[0, 1, 2], [1, 0, 2], [2, 1, 0], [3, 2, 4], [4, 3, 2]]
+    assert d2.tolist() == [[0, 1, 9], [0, 1, 4], [0, 4, 9], [0, 9, 16], [0, 16, 49]]
+
+
+def test_knn_duplicates_ordered_by_index():
+    x = np.zeros((6, 3), np.float32)
+    x[4] = [1, 0, 0]
+    ids, d2 = oracle.knn(x, 5)
+    for i in range(6):
+        if i == 4:
+            assert ids[i].tolist() == [4, 0, 1, 2, 3]
+        else:
+            assert ids[i].tolist() == [0, 1, 2, 3, 5]
+            assert np.all(d2[i] == 0)
+
+
+def test_knn_matches_pure_python_loops():
+    rng = np.random.default_rng(11)
+    x = rng.integers(0, 4, size=(40, 3)).astype(np.float32)  # many exact ties
+    ids, _ = oracle.knn(x, 7)
+    assert ids.tolist() == oracle.knn_py(x, 7)
+
+
+def test_knn_consistent_with_join_rows():
+    x = datagen.generate(2, n=800)
+    k = 10
+    ids, d2 = oracle.knn(x, k)
+    for i in range(0, 800, 37):
+        r = float(np.sqrt(d2[i, -1]))
+        rp, cols, _, _ = oracle.rows(x, np.float32(r) * np.float32(1.0001), [i], band=0.0)
+        assert set(ids[i].tolist()) <= set(cols.tolist())
+        assert len(cols) >= k
+
+
+def test_knn_matches_sklearn_brute_force():
+    nn = pytest.importorskip("sklearn.neighbors")
+    x = datagen.generate(4, n=500)
+    ids, d2 = oracle.knn(x, 8)
+    ref = nn.NearestNeighbors(n_neighbors=8, algorithm="brute").fit(x.astype(np.float64))
+    dist, rid = ref.kneighbors(x.astype(np.float64))
+    assert np.array_equal(ids, rid)
+    assert np.allclose(d2, dist ** 2, rtol=1e-9, atol=1e-12)
