@@ -104,12 +104,13 @@ hiss_join_queries = _sig("hiss_join_queries", ctypes.c_int,
 hiss_count_queries = _sig("hiss_count_queries", ctypes.c_int, [_p, _p, _i64, _f32, _p])
 hiss_exclusive_scan_noalloc = _sig("hiss_exclusive_scan_noalloc", ctypes.c_int, [_p, _p, _p, _i64])
 hiss_gram_tf32 = _sig("hiss_gram_tf32", ctypes.c_int, [_p, _p, _p, _i32, _p])
+hiss_knn = _sig("hiss_knn", ctypes.c_int, [_p, _i32, _f32, _p, _p])
 
 EXPORTED = ["hiss_create", "hiss_destroy", "hiss_build", "hiss_build_host", "hiss_count", "hiss_join",
             "hiss_index", "hiss_last_stats", "hiss_launch_count", "hiss_strerror", "hiss_last_cuda_error",
             "hiss_set_option", "hiss_sort_pairs", "hiss_exclusive_scan", "hiss_mask_positions",
             "hiss_exclusive_scan_noalloc", "hiss_work_profile", "hiss_join_queries", "hiss_count_queries",
-            "hiss_gram_tf32"]
+            "hiss_gram_tf32", "hiss_knn"]
 
 
 class HissError(RuntimeError):
@@ -337,6 +338,15 @@ class Join:
 
     def set_alloc_limit(self, nbytes):
         _check(hiss_set_option(self._h, HISS_OPT_ALLOC_LIMIT, int(nbytes)), self._h, "hiss_set_option")
+
+    def knn(self, k, eps0=0.0):
+        """Exact k nearest neighbours of every point (hiss_knn): (ids int64
+        (n, k), squared distances float32 (n, k)) as torch CUDA tensors."""
+        import torch
+        ids = torch.empty((self.n, k), dtype=torch.int64, device="cuda")
+        d2 = torch.empty((self.n, k), dtype=torch.float32, device="cuda")
+        _check(hiss_knn(self._h, int(k), float(eps0), ids.data_ptr(), d2.data_ptr()), self._h, "hiss_knn")
+        return ids, d2
 
     def set_refine(self, tensor_cores):
         """Select the refinement: CUDA cores (default) or the tensor-core

@@ -76,6 +76,9 @@ struct hiss_ctx {
     DBuf q_xv, q_xs, q_ids, q_cell_of_row, q_cell_start, q_cell_key, q_nbr, q_nbr_cnt, q_bound, q_work_key, q_cell_idx,
         q_work;
 
+    // exact kNN: per-batch pair scratch, done flags, active query ids
+    DBuf k_keys, k_vals, k_keys_alt, k_vals_alt, k_sort_tmp, k_d2, k_prow, k_done, k_active;
+
     hiss_stats st{};
     cudaEvent_t ev[8] = {};
 };
@@ -697,11 +700,13 @@ int do_join(hiss_ctx *ctx, float eps, size_t batch_bytes, const hiss_out *out)
 }
 
 // ---- semi-join: the query side built from separate query points -------------------
+// d_queries: nq x d rows in the dataset's original dimension order, or NULL
+// when ctx->q_xv already holds the nq rows permuted and padded (kNN rounds).
 int build_query_side(hiss_ctx *ctx, const float *d_queries, int64_t nq, QuerySide *out)
 {
     cudaStream_t s = ctx->stream;
     const int d = ctx->d, d4 = ctx->d4;
-    ST(ensure(ctx, ctx->q_xv, sizeof(float) * (size_t)nq * d4));
+    if (d_queries) ST(ensure(ctx, ctx->q_xv, sizeof(float) * (size_t)nq * d4));
     ST(ensure(ctx, ctx->q_xs, sizeof(float) * (size_t)nq * d4));
     ST(ensure(ctx, ctx->q_ids, 4 * (size_t)nq));
     ST(ensure(ctx, ctx->q_cell_of_row, 4 * (size_t)nq));
@@ -713,7 +718,8 @@ int build_query_side(hiss_ctx *ctx, const float *d_queries, int64_t nq, QuerySid
     ST(ensure(ctx, ctx->flag, 4 * (size_t)nq));
     ST(ensure(ctx, ctx->flag_scan, 4 * (size_t)(nq + 1)));
     ST(ensure(ctx, ctx->scan_tmp, 8 * (size_t)scan_tmp_elems(nq + 1) + 64));
-    CK(permute_pad(d_queries, nq, d, d4, as<int32_t>(ctx->perm_d), as<float>(ctx->q_xv), s, &ctx->launches));
+    if (d_queries)
+        CK(permute_pad(d_queries, nq, d, d4, as<int32_t>(ctx->perm_d), as<float>(ctx->q_xv), s, &ctx->launches));
     int64_t cellmax = 0;
     for (int k = 0; k < ctx->gp.ndim; ++k) {
         const int dim = ctx->perm[k];
@@ -806,6 +812,152 @@ int do_semi(hiss_ctx *ctx, const float *d_queries, int64_t nq, float eps, size_t
     return run_batches(ctx, qs, eps, batch_bytes, out, ms_index, launches0);
 }
 
+
+// ---- exact kNN by epsilon expansion -------------------------------------------------
+constexpr size_t kKnnBatchBytes = size_t(64) << 20;  // mask per join batch: < 2^29 candidates
+constexpr int kKnnMaxRounds = 256;
+
+struct KnnState {
+    hiss_ctx *ctx;
+    int semi;                   // 0: first round (self-join, query rows = xs); 1: semi-join (query rows = q_xs)
+    const int32_t *query_map;   // round's query index -> point id (NULL in the first round)
+    int k;
+    int64_t *out_ids;
+    float *out_d2;
+    int status;
+};
+
+// Called by run_batches for every CSR batch of a kNN round (device pointers).
+int knn_on_batch(void *user, const hiss_batch *b)
+{
+    KnnState *st = static_cast<KnnState *>(user);
+    hiss_ctx *ctx = st->ctx;
+    cudaStream_t s = ctx->stream;
+    const int64_t nnz = b->nnz;
+    if (nnz >= (int64_t(1) << 30)) {
+        st->status = HISS_E_OVERFLOW;
+        return 1;
+    }
+    int rc = HISS_OK;
+    if ((rc = ensure(ctx, ctx->k_keys, 8 * (size_t)nnz)) || (rc = ensure(ctx, ctx->k_vals, 4 * (size_t)nnz)) ||
+        (rc = ensure(ctx, ctx->k_keys_alt, 8 * (size_t)nnz)) || (rc = ensure(ctx, ctx->k_vals_alt, 4 * (size_t)nnz)) ||
+        (rc = ensure(ctx, ctx->k_sort_tmp, sort_tmp_bytes(nnz))) || (rc = ensure(ctx, ctx->k_d2, 4 * (size_t)nnz)) ||
+        (rc = ensure(ctx, ctx->k_prow, 4 * (size_t)nnz))) {
+        st->status = rc;
+        return 1;
+    }
+    KnnBatchArgs a{};
+    // the query side's buffers are (re)allocated inside the round: read them now
+    a.xq = st->semi ? as<float>(ctx->q_xs) : as<float>(ctx->xs);
+    a.xv = as<float>(ctx->xv);
+    a.row_ptr = b->row_ptr;
+    a.cols = b->cols;
+    a.query_rows = b->query_rows;
+    a.query_ids = b->query_ids;
+    a.query_map = st->query_map;
+    a.nq = b->nq;
+    a.nnz = nnz;
+    a.d4 = ctx->d4;
+    a.k = st->k;
+    a.d2 = as<float>(ctx->k_d2);
+    a.prow = as<int32_t>(ctx->k_prow);
+    a.keys = as<uint64_t>(ctx->k_keys);
+    a.vals = as<uint32_t>(ctx->k_vals);
+    a.out_ids = st->out_ids;
+    a.out_d2 = st->out_d2;
+    a.done = as<int8_t>(ctx->k_done);
+    cudaError_t e = knn_batch_pairs(a, s, &ctx->launches);
+    int in_alt = 0;
+    // by neighbour id, then stably by (row, squared distance)
+    if (e == cudaSuccess)
+        e = sort_pairs(a.keys, a.vals, as<uint64_t>(ctx->k_keys_alt), as<uint32_t>(ctx->k_vals_alt), nnz, 31,
+                       ctx->k_sort_tmp.p, as<int>(ctx->flags), s, &ctx->launches, &in_alt);
+    if (in_alt) {
+        a.keys = as<uint64_t>(ctx->k_keys_alt);
+        a.vals = as<uint32_t>(ctx->k_vals_alt);
+    }
+    if (e == cudaSuccess) e = knn_batch_rekey(a, s, &ctx->launches);
+    uint64_t *ka = in_alt ? as<uint64_t>(ctx->k_keys) : as<uint64_t>(ctx->k_keys_alt);
+    uint32_t *va = in_alt ? as<uint32_t>(ctx->k_vals) : as<uint32_t>(ctx->k_vals_alt);
+    in_alt = 0;
+    if (e == cudaSuccess)
+        e = sort_pairs(a.keys, a.vals, ka, va, nnz, 32 + bit_length(b->nq), ctx->k_sort_tmp.p, as<int>(ctx->flags), s,
+                       &ctx->launches, &in_alt);
+    if (in_alt) a.vals = va;
+    if (e == cudaSuccess) e = knn_batch_take(a, s, &ctx->launches);
+    if (e != cudaSuccess) {
+        st->status = fail_cuda(ctx, e);
+        return 1;
+    }
+    return 0;
+}
+
+int do_knn(hiss_ctx *ctx, int32_t k, float eps0, int64_t *out_ids, float *out_d2)
+{
+    const int64_t n = ctx->n;
+    const int d = ctx->d;
+    cudaStream_t s = ctx->stream;
+    // a radius that holds every point: the dataset's diameter (fp64, padded)
+    double diam2 = 0.0;
+    for (int j = 0; j < d; ++j) {
+        const double e = ctx->stats[1 * (size_t)d + j] - ctx->stats[0 * (size_t)d + j];
+        diam2 += e * e;
+    }
+    const float diam = (float)(std::sqrt(diam2) * (1.0 + 1e-3) + 1e-30);
+    float eps = eps0;
+    if (!(eps > 0.0f)) {
+        // start from the spacing of n points over the three index dimensions
+        double ext = 0.0;
+        for (int j = 0; j < std::min(d, 3); ++j) {
+            const int dim = ctx->perm[j];
+            ext = std::max(ext, ctx->stats[1 * (size_t)d + dim] - ctx->stats[0 * (size_t)d + dim]);
+        }
+        eps = (float)(0.5 * ext * std::pow((double)k / (double)n, 1.0 / std::min(d, 3)));
+        if (!(eps > 0.0f)) eps = diam;
+    }
+    ST(ensure(ctx, ctx->k_done, (size_t)n));
+    ST(ensure(ctx, ctx->k_active, 4 * (size_t)n));
+    CK(cudaMemsetAsync(ctx->k_done.p, 0, (size_t)n, s));
+    std::vector<int8_t> done(n);
+    std::vector<uint32_t> active;
+    hiss_out out{};
+    out.mode = HISS_OUT_CSR;
+    out.copy_to_host = 0;
+    out.on_batch = knn_on_batch;
+    KnnState st{ctx, 0, nullptr, k, out_ids, out_d2, HISS_OK};
+    out.user = &st;
+    for (int round = 0; round < kKnnMaxRounds; ++round) {
+        int rc;
+        if (round == 0) {
+            st.semi = 0;
+            st.query_map = nullptr;
+            rc = do_join(ctx, eps, kKnnBatchBytes, &out);
+        } else {
+            // the queries still short of k neighbours, as a semi-join against the data
+            const int64_t nq = (int64_t)active.size();
+            ST(ensure(ctx, ctx->q_xv, sizeof(float) * (size_t)nq * ctx->d4));
+            ST(ensure(ctx, ctx->q_ids, 4 * (size_t)nq));
+            CK(cudaMemcpyAsync(ctx->k_active.p, active.data(), 4 * (size_t)nq, cudaMemcpyHostToDevice, s));
+            CK(gather_rows(as<float>(ctx->xv), as<uint32_t>(ctx->k_active), nq, ctx->d4, as<float>(ctx->q_xv),
+                           as<int32_t>(ctx->q_ids), s, &ctx->launches));
+            st.semi = 1;
+            st.query_map = as<int32_t>(ctx->k_active);
+            rc = do_semi(ctx, nullptr, nq, eps, kKnnBatchBytes, &out, nullptr);
+        }
+        if (rc == HISS_E_CALLBACK) return st.status != HISS_OK ? st.status : HISS_E_CUDA;
+        if (rc != HISS_OK) return rc;
+        CK(cudaMemcpyAsync(done.data(), ctx->k_done.p, (size_t)n, cudaMemcpyDeviceToHost, s));
+        ST(sync(ctx));
+        active.clear();
+        for (int64_t i = 0; i < n; ++i)
+            if (!done[i]) active.push_back((uint32_t)i);
+        if (active.empty()) return HISS_OK;
+        if (eps >= diam) return HISS_E_STATE;  // cannot happen: eps = diameter holds every point
+        eps = std::min(diam, std::max(eps * 1.41421356f, std::nextafter(eps, INFINITY)));
+    }
+    return HISS_E_OVERFLOW;
+}
+
 }  // namespace
 
 // ============================================================================
@@ -853,7 +1005,9 @@ void hiss_destroy(hiss_ctx *ctx)
                    &ctx->query_ids, &ctx->query_rows, &ctx->cand, &ctx->mask_row_ptr, &ctx->t_keys_alt,
                    &ctx->t_vals_alt, &ctx->t_sort_tmp, &ctx->t_scan_tmp, &ctx->q_xv, &ctx->q_xs, &ctx->q_ids,
                    &ctx->q_cell_of_row, &ctx->q_cell_start, &ctx->q_cell_key, &ctx->q_nbr, &ctx->q_nbr_cnt,
-                   &ctx->q_bound, &ctx->q_work_key, &ctx->q_cell_idx, &ctx->q_work};
+                   &ctx->q_bound, &ctx->q_work_key, &ctx->q_cell_idx, &ctx->q_work, &ctx->k_keys,
+                   &ctx->k_vals, &ctx->k_keys_alt, &ctx->k_vals_alt, &ctx->k_sort_tmp, &ctx->k_d2, &ctx->k_prow,
+                   &ctx->k_done, &ctx->k_active};
     for (DBuf *b : all) release(ctx, *b);
     cudaStreamSynchronize(ctx->stream);
     if (ctx->h_pinned) cudaFreeHost(ctx->h_pinned);
@@ -1081,6 +1235,17 @@ int hiss_gram_tf32(hiss_ctx *ctx, const float *d_a, const float *d_b, int32_t k,
     CK(gram_tf32(d_a, d_b, k, d_out, as<int>(ctx->flags), ctx->stream, &ctx->launches));
     ST(sync(ctx));
     return check_flags(ctx);
+}
+
+int hiss_knn(hiss_ctx *ctx, int32_t k, float eps0, int64_t *d_ids, float *d_dist2)
+{
+    ST(enter(ctx));
+    if (!ctx->built) return HISS_E_STATE;
+    if (!d_ids || k < 1 || (int64_t)k > ctx->n || std::isnan(eps0) || std::isinf(eps0)) return HISS_E_ARG;
+    const int64_t launches0 = ctx->launches;
+    const int rc = do_knn(ctx, k, eps0, d_ids, d_dist2);
+    ctx->st.kernel_launches = ctx->launches - launches0;
+    return rc;
 }
 
 }  // extern "C"

@@ -145,6 +145,32 @@ cudaError_t compact(const CompactArgs &a, cudaStream_t s, int64_t *launches);
 cudaError_t mask_positions(const uint32_t *words, int64_t nbits, int64_t *pos, int64_t *count,
                            int64_t *tmp, cudaStream_t s, int64_t *launches);
 
+// ---- exact kNN by epsilon expansion (knn.cu) --------------------------------------
+// One CSR batch of an epsilon join: per pair p of row r (row_ptr), the float32
+// squared distance d2[p] between query row query_rows[r] of xq and data point
+// cols[p] of xv (original order, variance-ordered dimensions).
+struct KnnBatchArgs {
+    const float *xq;             // query rows (index order of the query side), row stride d4
+    const float *xv;             // data points in original order, row stride d4
+    const int64_t *row_ptr;      // [nq + 1]
+    const int32_t *cols;         // [nnz] neighbour ids
+    const int32_t *query_rows;   // [nq] row of each query in xq
+    const int64_t *query_ids;    // [nq] id of each query in the join's query set
+    const int32_t *query_map;    // query set -> point id (NULL: identity)
+    int64_t nq, nnz;
+    int d4, k;
+    float *d2;                   // [nnz] scratch: squared distances
+    int32_t *prow;               // [nnz] scratch: row of each pair
+    uint64_t *keys;              // [nnz] sort keys
+    uint32_t *vals;              // [nnz] sort values (pair index)
+    int64_t *out_ids;            // [n * k]
+    float *out_d2;               // [n * k] or NULL
+    int8_t *done;                // [n] set to 1 for queries completed in this batch
+};
+cudaError_t knn_batch_pairs(const KnnBatchArgs &a, cudaStream_t s, int64_t *launches);   // d2, prow, keys = col, vals = p
+cudaError_t knn_batch_rekey(const KnnBatchArgs &a, cudaStream_t s, int64_t *launches);   // keys = (prow << 32) | d2 bits
+cudaError_t knn_batch_take(const KnnBatchArgs &a, cudaStream_t s, int64_t *launches);    // first k per row with >= k pairs
+
 // ---- tensor cores (refine_tc.cu) ----------------------------------------------
 // Refinement of a batch with the squared distances from TF32 Gram matrices on
 // the tensor cores and an exact float32 recheck of every undecided pair;

@@ -169,6 +169,22 @@ int hiss_join_queries(hiss_ctx *ctx, const float *d_queries, int64_t nq, float e
  * around the query's cell, >= its true neighbour count. */
 int hiss_count_queries(hiss_ctx *ctx, const float *d_queries, int64_t nq, float eps, int64_t *d_counts);
 
+/* Exact k nearest neighbours by epsilon expansion (RT-HiSS names exact kNN
+ * as a use of the epsilon join: repeat the join with a growing eps for the
+ * queries that have fewer than k neighbours, then keep the k nearest).  For
+ * every point of the dataset (the point itself included, at distance 0):
+ * d_ids (device int64[n * k], row i = point i) receives the ids of its k
+ * nearest points by float32 squared distance summed in variance order,
+ * increasing, equal distances by increasing id; d_dist2 (device
+ * float32[n * k], may be NULL) receives those squared distances.  Round 1 is
+ * the self-join for eps0 (eps0 <= 0: a start from the point spacing over the
+ * three index dimensions); each later round multiplies eps by sqrt(2), capped
+ * at the dataset's diameter, and semi-joins only the points still short of k
+ * neighbours.  A point is finished in the first round where it has at least
+ * k neighbours within eps, which holds its k nearest.  1 <= k <= n.  Join
+ * batches are limited to 64 MiB of result mask. */
+int hiss_knn(hiss_ctx *ctx, int32_t k, float eps0, int64_t *d_ids, float *d_dist2);
+
 /* Read-only view of the index built for the last eps (device pointers owned
  * by the context, valid until the next build or a call with another eps). */
 typedef struct {
