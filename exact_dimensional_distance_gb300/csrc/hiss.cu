@@ -814,7 +814,7 @@ int do_semi(hiss_ctx *ctx, const float *d_queries, int64_t nq, float eps, size_t
 
 
 // ---- exact kNN by epsilon expansion -------------------------------------------------
-constexpr size_t kKnnBatchBytes = size_t(64) << 20;  // mask per join batch: < 2^29 candidates
+constexpr size_t kKnnBatchBytes = size_t(1) << 30;   // mask per join batch
 constexpr int kKnnMaxRounds = 256;
 
 struct KnnState {
@@ -827,36 +827,31 @@ struct KnnState {
     int status;
 };
 
-// Called by run_batches for every CSR batch of a kNN round (device pointers).
-int knn_on_batch(void *user, const hiss_batch *b)
+// A group of rows of one batch whose pairs fit the group limit (a single row
+// may exceed it; every count stays below the radix sort's 2^30).
+int knn_group(KnnState *st, const hiss_batch *b, int64_t r0, int64_t r1, int64_t pair0, int64_t nnz)
 {
-    KnnState *st = static_cast<KnnState *>(user);
     hiss_ctx *ctx = st->ctx;
     cudaStream_t s = ctx->stream;
-    const int64_t nnz = b->nnz;
-    if (nnz >= (int64_t(1) << 30)) {
-        st->status = HISS_E_OVERFLOW;
-        return 1;
-    }
-    int rc = HISS_OK;
-    if ((rc = ensure(ctx, ctx->k_keys, 8 * (size_t)nnz)) || (rc = ensure(ctx, ctx->k_vals, 4 * (size_t)nnz)) ||
-        (rc = ensure(ctx, ctx->k_keys_alt, 8 * (size_t)nnz)) || (rc = ensure(ctx, ctx->k_vals_alt, 4 * (size_t)nnz)) ||
-        (rc = ensure(ctx, ctx->k_sort_tmp, sort_tmp_bytes(nnz))) || (rc = ensure(ctx, ctx->k_d2, 4 * (size_t)nnz)) ||
-        (rc = ensure(ctx, ctx->k_prow, 4 * (size_t)nnz))) {
-        st->status = rc;
-        return 1;
-    }
+    ST(ensure(ctx, ctx->k_keys, 8 * (size_t)nnz));
+    ST(ensure(ctx, ctx->k_vals, 4 * (size_t)nnz));
+    ST(ensure(ctx, ctx->k_keys_alt, 8 * (size_t)nnz));
+    ST(ensure(ctx, ctx->k_vals_alt, 4 * (size_t)nnz));
+    ST(ensure(ctx, ctx->k_sort_tmp, sort_tmp_bytes(nnz)));
+    ST(ensure(ctx, ctx->k_d2, 4 * (size_t)nnz));
+    ST(ensure(ctx, ctx->k_prow, 4 * (size_t)nnz));
     KnnBatchArgs a{};
     // the query side's buffers are (re)allocated inside the round: read them now
     a.xq = st->semi ? as<float>(ctx->q_xs) : as<float>(ctx->xs);
     a.xv = as<float>(ctx->xv);
-    a.row_ptr = b->row_ptr;
+    a.row_ptr = b->row_ptr + r0;
     a.cols = b->cols;
-    a.query_rows = b->query_rows;
-    a.query_ids = b->query_ids;
+    a.query_rows = b->query_rows + r0;
+    a.query_ids = b->query_ids + r0;
     a.query_map = st->query_map;
-    a.nq = b->nq;
+    a.nq = r1 - r0;
     a.nnz = nnz;
+    a.pair0 = pair0;
     a.d4 = ctx->d4;
     a.k = st->k;
     a.d2 = as<float>(ctx->k_d2);
@@ -866,27 +861,44 @@ int knn_on_batch(void *user, const hiss_batch *b)
     a.out_ids = st->out_ids;
     a.out_d2 = st->out_d2;
     a.done = as<int8_t>(ctx->k_done);
-    cudaError_t e = knn_batch_pairs(a, s, &ctx->launches);
-    int in_alt = 0;
+    CK(knn_batch_pairs(a, s, &ctx->launches));
     // by neighbour id, then stably by (row, squared distance)
-    if (e == cudaSuccess)
-        e = sort_pairs(a.keys, a.vals, as<uint64_t>(ctx->k_keys_alt), as<uint32_t>(ctx->k_vals_alt), nnz, 31,
-                       ctx->k_sort_tmp.p, as<int>(ctx->flags), s, &ctx->launches, &in_alt);
+    int in_alt = 0;
+    CK(sort_pairs(a.keys, a.vals, as<uint64_t>(ctx->k_keys_alt), as<uint32_t>(ctx->k_vals_alt), nnz, 31,
+                  ctx->k_sort_tmp.p, as<int>(ctx->flags), s, &ctx->launches, &in_alt));
     if (in_alt) {
         a.keys = as<uint64_t>(ctx->k_keys_alt);
         a.vals = as<uint32_t>(ctx->k_vals_alt);
     }
-    if (e == cudaSuccess) e = knn_batch_rekey(a, s, &ctx->launches);
+    CK(knn_batch_rekey(a, s, &ctx->launches));
     uint64_t *ka = in_alt ? as<uint64_t>(ctx->k_keys) : as<uint64_t>(ctx->k_keys_alt);
     uint32_t *va = in_alt ? as<uint32_t>(ctx->k_vals) : as<uint32_t>(ctx->k_vals_alt);
-    in_alt = 0;
-    if (e == cudaSuccess)
-        e = sort_pairs(a.keys, a.vals, ka, va, nnz, 32 + bit_length(b->nq), ctx->k_sort_tmp.p, as<int>(ctx->flags), s,
-                       &ctx->launches, &in_alt);
+    CK(sort_pairs(a.keys, a.vals, ka, va, nnz, 32 + bit_length(a.nq), ctx->k_sort_tmp.p, as<int>(ctx->flags), s,
+                  &ctx->launches, &in_alt));
     if (in_alt) a.vals = va;
-    if (e == cudaSuccess) e = knn_batch_take(a, s, &ctx->launches);
-    if (e != cudaSuccess) {
-        st->status = fail_cuda(ctx, e);
+    CK(knn_batch_take(a, s, &ctx->launches));
+    return HISS_OK;
+}
+
+// Called by run_batches for every CSR batch of a kNN round (device pointers).
+int knn_on_batch(void *user, const hiss_batch *b)
+{
+    KnnState *st = static_cast<KnnState *>(user);
+    hiss_ctx *ctx = st->ctx;
+    std::vector<int64_t> rp((size_t)b->nq + 1);
+    int rc = HISS_OK;
+    if (cudaMemcpyAsync(rp.data(), b->row_ptr, 8 * rp.size(), cudaMemcpyDeviceToHost, ctx->stream) != cudaSuccess)
+        rc = fail_cuda(ctx, cudaGetLastError());
+    if (rc == HISS_OK) rc = sync(ctx);
+    constexpr int64_t kMaxPairs = int64_t(1) << 27;  // about 3.8 GB of sort scratch per group
+    for (int64_t r0 = 0; rc == HISS_OK && r0 < b->nq;) {
+        int64_t r1 = r0 + 1;  // one row never exceeds n < 2^30 pairs
+        while (r1 < b->nq && rp[r1 + 1] - rp[r0] <= kMaxPairs) ++r1;
+        rc = knn_group(st, b, r0, r1, rp[r0], rp[r1] - rp[r0]);
+        r0 = r1;
+    }
+    if (rc != HISS_OK) {
+        st->status = rc;
         return 1;
     }
     return 0;

@@ -146,7 +146,9 @@ cudaError_t mask_positions(const uint32_t *words, int64_t nbits, int64_t *pos, i
                            int64_t *tmp, cudaStream_t s, int64_t *launches);
 
 // ---- exact kNN by epsilon expansion (knn.cu) --------------------------------------
-// One CSR batch of an epsilon join: per pair p of row r (row_ptr), the float32
+// A group of rows of one CSR batch of an epsilon join (row_ptr, query_rows and
+// query_ids point at the group's first row; scratch arrays are indexed from the
+// group's first pair): per pair p of row r, the float32
 // squared distance d2[p] between query row query_rows[r] of xq and data point
 // cols[p] of xv (original order, variance-ordered dimensions).
 struct KnnBatchArgs {
@@ -158,6 +160,7 @@ struct KnnBatchArgs {
     const int64_t *query_ids;    // [nq] id of each query in the join's query set
     const int32_t *query_map;    // query set -> point id (NULL: identity)
     int64_t nq, nnz;
+    int64_t pair0;               // pairs of this group start at cols[pair0] (= row_ptr[0])
     int d4, k;
     float *d2;                   // [nnz] scratch: squared distances
     int32_t *prow;               // [nnz] scratch: row of each pair

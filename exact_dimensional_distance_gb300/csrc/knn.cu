@@ -23,10 +23,10 @@ __global__ void __launch_bounds__(kKnnWarps * 32) k_knn_pairs(KnnBatchArgs a)
     const int lane = threadIdx.x & 31;
     const int64_t r = (int64_t)blockIdx.x * kKnnWarps + (threadIdx.x >> 5);
     if (r >= a.nq) return;
-    const int64_t p0 = a.row_ptr[r], p1 = a.row_ptr[r + 1];
+    const int64_t p0 = a.row_ptr[r] - a.pair0, p1 = a.row_ptr[r + 1] - a.pair0;
     const float *q = a.xq + (int64_t)a.query_rows[r] * a.d4;
     for (int64_t p = p0 + lane; p < p1; p += 32) {
-        const int32_t c = a.cols[p];
+        const int32_t c = a.cols[a.pair0 + p];
         const float *x = a.xv + (int64_t)c * a.d4;
         float s = 0.0f;
         for (int k = 0; k < a.d4; k += 4) {
@@ -64,12 +64,12 @@ __global__ void k_knn_take(KnnBatchArgs a)
     const int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (r >= a.nq) return;
-    const int64_t p0 = a.row_ptr[r], cnt = a.row_ptr[r + 1] - p0;
+    const int64_t p0 = a.row_ptr[r] - a.pair0, cnt = a.row_ptr[r + 1] - a.row_ptr[r];
     if (cnt < a.k) return;
     const int64_t id = a.query_map ? (int64_t)a.query_map[a.query_ids[r]] : a.query_ids[r];
     for (int t = lane; t < a.k; t += 32) {
         const uint32_t p = a.vals[p0 + t];
-        a.out_ids[id * a.k + t] = a.cols[p];
+        a.out_ids[id * a.k + t] = a.cols[a.pair0 + p];
         if (a.out_d2) a.out_d2[id * a.k + t] = a.d2[p];
     }
     if (lane == 0) a.done[id] = 1;

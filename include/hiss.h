@@ -182,7 +182,8 @@ int hiss_count_queries(hiss_ctx *ctx, const float *d_queries, int64_t nq, float 
  * at the dataset's diameter, and semi-joins only the points still short of k
  * neighbours.  A point is finished in the first round where it has at least
  * k neighbours within eps, which holds its k nearest.  1 <= k <= n.  Join
- * batches are limited to 64 MiB of result mask. */
+ * batches hold up to 1 GiB of result mask; their pairs are ranked in groups
+ * of rows of at most 2^27 pairs (one longer row forms its own group). */
 int hiss_knn(hiss_ctx *ctx, int32_t k, float eps0, int64_t *d_ids, float *d_dist2);
 
 /* Read-only view of the index built for the last eps (device pointers owned
