@@ -40,7 +40,10 @@ constexpr int kQueryWarps = 4, kCandWarps = 2;
 constexpr int kComputeWarps = kQueryWarps * kCandWarps;
 constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kRefineThreads = kComputeThreads + 32;
-constexpr int kCH = 8192;  // candidates per unit
+#ifndef HISS_REFINE_CHUNK
+#define HISS_REFINE_CHUNK 8192
+#endif
+constexpr int kCH = HISS_REFINE_CHUNK;  // candidates per unit (a multiple of 64)
 
 // Per-thread block MQ x MP: 8 x 4 up to d4 = 64 (tiles of 128 queries x 64
 // candidates), 4 x 4 above (64 x 64), so that two blocks fit per SM.
