@@ -63,7 +63,7 @@ struct hiss_ctx {
     uint32_t *order = nullptr;
 
     // batches
-    DBuf boundaries, binfo, nb_d, mask, qcount, row_ptr, cols, query_ids, query_rows, cand, mask_row_ptr;
+    DBuf boundaries, binfo, nb_d, mask, occ, qcount, row_ptr, cols, query_ids, query_rows, cand, mask_row_ptr;
 
     // host staging for copy_to_host
     void *h_pinned = nullptr;
@@ -532,6 +532,7 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
         max_nq = std::max(max_nq, info[4 * (b + 1) + 2] - info[4 * b + 2]);
     }
     ST(ensure(ctx, ctx->mask, 4 * (size_t)max_words));
+    ST(ensure(ctx, ctx->occ, 4 * (size_t)(max_words / 32 + 2)));
     ST(ensure(ctx, ctx->qcount, 4 * (size_t)(max_nq + 1)));
     ST(ensure(ctx, ctx->row_ptr, 8 * (size_t)(max_nq + 1)));
     ST(ensure(ctx, ctx->query_ids, 8 * (size_t)max_nq));
@@ -549,6 +550,10 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
         const int64_t nq = hi[2] - lo[2];
         const int64_t nwords = hi[0] - lo[0];
         CK(cudaMemsetAsync(ctx->qcount.p, 0, 4 * (size_t)nq, s));
+        // the refinement stores only nonzero mask words and marks them in occ;
+        // the raw-mask output needs the zero words too
+        CK(cudaMemsetAsync(ctx->occ.p, 0, 4 * (size_t)(nwords / 32 + 2), s));
+        if (mode == HISS_OUT_MASK) CK(cudaMemsetAsync(ctx->mask.p, 0, 4 * (size_t)nwords, s));
         RefineArgs ra{};
         ra.xs = as<float>(ctx->xs);
         ra.xq = qs.xq;
@@ -569,6 +574,7 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
         ra.word0 = lo[0];
         ra.q0 = lo[2];
         ra.mask = as<uint32_t>(ctx->mask);
+        ra.occ = as<uint32_t>(ctx->occ);
         ra.qcount = as<int32_t>(ctx->qcount);
         ra.d4 = ctx->d4;
         ra.d = ctx->d;
@@ -597,6 +603,7 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
         ca.q0 = ra.q0;
         ca.nq = nq;
         ca.mask = ra.mask;
+        ca.occ = ra.occ;
         ca.query_ids = as<int64_t>(ctx->query_ids);
         ca.query_rows = as<int32_t>(ctx->query_rows);
         int64_t nnz = 0;
@@ -1013,7 +1020,7 @@ void hiss_destroy(hiss_ctx *ctx)
                    &ctx->nbr_cnt, &ctx->bound, &ctx->work_key, &ctx->cell_idx, &ctx->work, &ctx->scan_tmp,
                    &ctx->sums2, &ctx->lpt_keys, &ctx->lpt_order, &ctx->ntiles, &ctx->tile_off, &ctx->tile_cell,
                    &ctx->tile_q0, &ctx->tile_nq, &ctx->tile_word, &ctx->tile_unit, &ctx->tile_qoff,
-                   &ctx->boundaries, &ctx->binfo, &ctx->nb_d, &ctx->mask, &ctx->qcount, &ctx->row_ptr, &ctx->cols,
+                   &ctx->boundaries, &ctx->binfo, &ctx->nb_d, &ctx->mask, &ctx->occ, &ctx->qcount, &ctx->row_ptr, &ctx->cols,
                    &ctx->query_ids, &ctx->query_rows, &ctx->cand, &ctx->mask_row_ptr, &ctx->t_keys_alt,
                    &ctx->t_vals_alt, &ctx->t_sort_tmp, &ctx->t_scan_tmp, &ctx->q_xv, &ctx->q_xs, &ctx->q_ids,
                    &ctx->q_cell_of_row, &ctx->q_cell_start, &ctx->q_cell_key, &ctx->q_nbr, &ctx->q_nbr_cnt,

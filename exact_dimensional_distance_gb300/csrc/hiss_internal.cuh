@@ -108,7 +108,8 @@ struct RefineArgs {
     int64_t t0, t1;             // batch: tiles [t0, t1)
     int64_t unit0, nunits;      // units of the batch
     int64_t word0, q0;          // batch origin in words and queries
-    uint32_t *mask;             // batch mask
+    uint32_t *mask;             // batch mask: only nonzero words are written
+    uint32_t *occ;              // occupancy: bit (w & 31) of occ[w >> 5] set when mask word w is nonzero (zeroed per batch)
     int32_t *qcount;            // [nq of batch] neighbour count per query (accumulated)
     int d4;
     int d;                      // true dimension (profile mode caps the last step at d)
@@ -134,6 +135,7 @@ struct CompactArgs {
     const int64_t *tile_qoff;
     int64_t t0, t1, word0, q0, nq;
     const uint32_t *mask;
+    const uint32_t *occ;        // occupancy bitmap of the mask (nonzero words)
     const int64_t *row_ptr;     // [nq+1] batch-relative
     int32_t *cols;              // CSR output (NULL: only query ids/rows/cand)
     int64_t *query_ids;         // [nq]

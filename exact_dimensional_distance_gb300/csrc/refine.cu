@@ -395,13 +395,13 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
                     const uint32_t w = __byte_perm(w01, w23, 0x5410);
                     if (lp == i) mine = w;
                 }
-                if (lp < MQ && qr < nq && wcol < W) {
-                    a.mask[row_word0 + (int64_t)qr * W4 + wcol] = mine;
+                if (lp < MQ && qr < nq && wcol < W && mine) {
+                    // only nonzero words are stored; the occupancy bitmap marks them
+                    const int64_t wi = row_word0 + (int64_t)qr * W4 + wcol;
+                    a.mask[wi] = mine;
+                    atomicOr(&a.occ[wi >> 5], 1u << (wi & 31));
                     my_count += __popc(mine);
                 }
-            } else if (lp < MQ && qr < nq && wcol < W) {
-                // no pair of the warp is within eps: a zero word for this lane's row
-                a.mask[row_word0 + (int64_t)qr * W4 + wcol] = 0u;
             }
         }
         __syncwarp();
@@ -489,36 +489,39 @@ __global__ void __launch_bounds__(kCompactWarps * 32) k_compact(const CompactArg
     if (lane < ns) s_vpre[warp][lane] = incl - sz;
     __syncwarp();
 
-    // rows are 16-byte aligned: each lane takes four words per step
-    const uint4 *mrow = reinterpret_cast<const uint4 *>(a.mask + woff);
+    // only the nonzero words of the row are visited: lane l takes occupancy
+    // word o = o0 + 32 s + l (bits = mask words 32 o .. 32 o + 31), clipped to
+    // the row's words [woff, woff + W)
     int32_t *out = a.cols + a.row_ptr[gq];
     int64_t run = 0;
-    for (int64_t w0 = 0; w0 < W; w0 += 128) {
-        const int64_t w = w0 + 4 * lane;
-        uint32_t wd[4] = {0u, 0u, 0u, 0u};
-        if (w < W) {
-            const uint4 v = mrow[w >> 2];
-            wd[0] = v.x;
-            wd[1] = w + 1 < W ? v.y : 0u;
-            wd[2] = w + 2 < W ? v.z : 0u;
-            wd[3] = w + 3 < W ? v.w : 0u;
+    const int64_t o0 = woff >> 5, o1 = (woff + W - 1) >> 5;
+    for (int64_t ob = o0; ob <= o1; ob += 32) {
+        const int64_t o = ob + lane;
+        uint32_t bits = 0;
+        if (o <= o1) {
+            bits = a.occ[o];
+            const int64_t wlo = 32 * o;
+            if (wlo < woff) bits &= ~0u << (int)(woff - wlo);
+            const int64_t n_in = woff + W - wlo;
+            if (n_in < 32) bits &= (1u << (int)n_in) - 1u;
         }
-        const int cnt = __popc(wd[0]) + __popc(wd[1]) + __popc(wd[2]) + __popc(wd[3]);
+        int cnt = 0;
+        for (uint32_t bb = bits; bb; bb &= bb - 1) cnt += __popc(a.mask[32 * o + __ffs(bb) - 1]);
         int ex = cnt;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, ex, o);
-            if (lane >= o) ex += v;
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, ex, off);
+            if (lane >= off) ex += v;
         }
         const int total = __shfl_sync(0xffffffffu, ex, 31);
         int64_t pos = run + ex - cnt;
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            uint32_t word = wd[h];
+        for (uint32_t bb = bits; bb; bb &= bb - 1) {
+            const int64_t w = 32 * o + __ffs(bb) - 1;
+            uint32_t word = a.mask[w];
             while (word) {
                 const int b = __ffs(word) - 1;
                 word &= word - 1;
-                const int64_t v = (w + h) * 32 + b;
+                const int64_t v = (w - woff) * 32 + b;
                 int l = 0, hh = ns - 1;
                 while (l < hh) {
                     const int m = (l + hh + 1) >> 1;

@@ -496,10 +496,14 @@ __global__ void __maxnreg__(96) k_refine_tc(const RefineArgs a, const TcConst cs
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_empty_d[buf]);
-            if (i < nq) {
+            const uint32_t nz = (words[0] ? 1u : 0u) | (words[1] ? 2u : 0u) | (words[2] ? 4u : 0u) | (words[3] ? 8u : 0u);
+            if (i < nq && nz) {
+                // only rows with a nonzero word store; the occupancy bitmap marks the
+                // nonzero words (4 consecutive words share one 32-bit occupancy word)
                 const int64_t v0 = vbeg + (int64_t)it * kTcRows;
-                *reinterpret_cast<uint4 *>(a.mask + row_word0 + (int64_t)i * W4 + (v0 >> 5)) =
-                    make_uint4(words[0], words[1], words[2], words[3]);
+                const int64_t wi = row_word0 + (int64_t)i * W4 + (v0 >> 5);
+                *reinterpret_cast<uint4 *>(a.mask + wi) = make_uint4(words[0], words[1], words[2], words[3]);
+                atomicOr(&a.occ[wi >> 5], nz << (wi & 31));
                 my_count += __popc(words[0]) + __popc(words[1]) + __popc(words[2]) + __popc(words[3]);
             }
         }
