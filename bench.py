@@ -198,7 +198,7 @@ def workload_config(args, eps):
         name, n = name + " (reduced instance for profiling)", args.n
     return {"workload": "%s N=%d d=%d mean_neighbours=%d" % (name, n, d, k), "n": n, "d": d, "eps": eps,
             "eps_hex": float(eps).hex(), "batch_bytes": args.batch_bytes, "l2": "flushed between steps",
-            "parallelism": "replica per GPU",
+            "parallelism": "one join sharded over the GPUs" if getattr(args, "shard", False) else "replica per GPU",
             "refine": "tensor cores (TF32 Gram prefilter + exact recheck)" if getattr(args, "refine", "cuda") == "tensor"
             else "CUDA cores"}
 
@@ -224,6 +224,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", type=int, default=2)
     ap.add_argument("--impl", default="hiss", choices=["hiss", "reference"])
+    ap.add_argument("--shard", action="store_true",
+                    help="under torchrun: each rank runs its shard of one join (strong scaling) instead of a replica")
     ap.add_argument("--refine", default="cuda", choices=["cuda", "tensor"],
                     help="refinement: CUDA cores (default) or the tensor-core prefilter with exact recheck")
     ap.add_argument("--batch-bytes", type=int, default=32 << 30)
@@ -265,13 +267,19 @@ def main():
         j.build(xd)
         j.count(eps, out=False)
         st_count = j.stats()
-        st_join = j.join(eps, args.batch_bytes)
+        if args.shard:
+            st_join = j.join_shard(eps, rank, world, args.batch_bytes)
+        else:
+            st_join = j.join(eps, args.batch_bytes)
         st_join["ms_index"] = st_count["ms_index"]
         st_join["ms_build"] = st_count["ms_build"]
         return st_join
 
     for _ in range(args.warmup):
         st = step()
+    total_units = None
+    if args.shard:
+        total_units = j.join(eps, args.batch_bytes)["refine_units"]  # the whole join, untimed
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     stats = []
     launches0 = j.launches()
@@ -303,6 +311,10 @@ def main():
     refine_ms = statistics.median(s["ms_refine"] for s in stats)
     refine_launches = st["batches"]
     dims_alg, dims_exec = j.work_profile(eps)
+    if args.shard and world > 1:
+        # the profile covers the whole join; this rank refined its share of the units
+        share = st["refine_units"] / float(total_units or 1)
+        dims_alg, dims_exec = dims_alg * share, dims_exec * share
     flops = 3.0 * dims_alg
     pk, pk_kind = peaks()
     peak = fp32_peak_tflops(pk.get("sm_max_mhz", 2070.0))
@@ -321,8 +333,8 @@ def main():
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": workload_config(args, eps), "gpu_launches": int(launches),
+            "scaling": "strong" if args.shard else "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": workload_config(args, eps), "gpu_launches": int(launches),
             "candidate_evals_per_s": world * cand * args.steps / t,
             "replicas": world,
             "pairs_per_step": pairs, "candidates_per_step": cand,
@@ -343,7 +355,10 @@ def main():
         def e2e_step():
             j.build(hx)
             j.count(eps, out=False)
-            j.join(eps, args.batch_bytes, edd.HISS_OUT_CSR, True, on_batch)
+            if args.shard:
+                j.join_shard(eps, rank, world, args.batch_bytes, edd.HISS_OUT_CSR, True, on_batch)
+            else:
+                j.join(eps, args.batch_bytes, edd.HISS_OUT_CSR, True, on_batch)
 
         e2e_step()
         torch.cuda.synchronize()

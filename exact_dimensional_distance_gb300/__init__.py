@@ -105,12 +105,14 @@ hiss_count_queries = _sig("hiss_count_queries", ctypes.c_int, [_p, _p, _i64, _f3
 hiss_exclusive_scan_noalloc = _sig("hiss_exclusive_scan_noalloc", ctypes.c_int, [_p, _p, _p, _i64])
 hiss_gram_tf32 = _sig("hiss_gram_tf32", ctypes.c_int, [_p, _p, _p, _i32, _p])
 hiss_knn = _sig("hiss_knn", ctypes.c_int, [_p, _i32, _f32, _p, _p])
+hiss_join_shard = _sig("hiss_join_shard", ctypes.c_int,
+                       [_p, _f32, ctypes.c_size_t, ctypes.POINTER(hiss_out), _i32, _i32])
 
 EXPORTED = ["hiss_create", "hiss_destroy", "hiss_build", "hiss_build_host", "hiss_count", "hiss_join",
             "hiss_index", "hiss_last_stats", "hiss_launch_count", "hiss_strerror", "hiss_last_cuda_error",
             "hiss_set_option", "hiss_sort_pairs", "hiss_exclusive_scan", "hiss_mask_positions",
             "hiss_exclusive_scan_noalloc", "hiss_work_profile", "hiss_join_queries", "hiss_count_queries",
-            "hiss_gram_tf32", "hiss_knn"]
+            "hiss_gram_tf32", "hiss_knn", "hiss_join_shard"]
 
 
 class HissError(RuntimeError):
@@ -240,6 +242,30 @@ class Join:
         if err:
             raise err[0]
         return rc
+
+    def join_shard(self, eps, rank, nranks, batch_bytes=0, mode=HISS_OUT_CSR, copy_to_host=False, on_batch=None):
+        """Shard rank of nranks of the self-join (hiss_join_shard); on_batch as
+        in ``join``.  Returns the stats dict."""
+        def call(fn):
+            out = hiss_out(mode, 1 if copy_to_host else 0, fn, None)
+            return hiss_join_shard(self._h, float(eps), int(batch_bytes), ctypes.byref(out), int(rank), int(nranks))
+
+        _check(self._run(call, on_batch), self._h, "hiss_join_shard")
+        return self.stats()
+
+    def join_shard_sets(self, eps, rank, nranks, batch_bytes=0):
+        """Rows of one shard as {query id: numpy array of neighbour ids}."""
+        res = {}
+
+        def take(b):
+            q = _host_array(b.query_ids, b.nq, np.int64)
+            rp = _host_array(b.row_ptr, b.nq + 1, np.int64)
+            cols = _host_array(b.cols, b.nnz, np.int32)
+            for i in range(b.nq):
+                res[int(q[i])] = cols[rp[i]:rp[i + 1]]
+
+        self.join_shard(eps, rank, nranks, batch_bytes, HISS_OUT_CSR, True, take)
+        return res
 
     def join_queries(self, queries, eps, batch_bytes=0, mode=HISS_OUT_CSR, copy_to_host=False, on_batch=None):
         """Semi-join of the query points (torch CUDA float32 (nq, d)) against

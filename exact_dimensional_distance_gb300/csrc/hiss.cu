@@ -493,8 +493,9 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 // Plan the batches over the current tiles and run them: refinement,
 // compaction, delivery and the callback, batch by batch.
+// tlo, thi: the query tiles (processing order) to run; thi < 0 means all.
 int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_bytes, const hiss_out *out,
-                double ms_index, int64_t launches0)
+                double ms_index, int64_t launches0, int64_t tlo = 0, int64_t thi = -1)
 {
     const int mode = out ? out->mode : HISS_OUT_CSR;
     const int to_host = out ? out->copy_to_host : 0;
@@ -508,14 +509,15 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
         batch_bytes = fr / 4;
     }
     const int64_t cap_words = (int64_t)(batch_bytes / 4);
-    const int64_t T = ctx->T;
+    if (thi < 0) thi = ctx->T;
+    const int64_t T = thi - tlo;  // tiles of this call; batch tile indices are relative to tlo
     ST(ensure(ctx, ctx->boundaries, 8 * (size_t)(T + 2)));
     ST(ensure(ctx, ctx->binfo, 32 * (size_t)(T + 2)));
     ST(ensure(ctx, ctx->nb_d, 64));
     CK(cudaMemsetAsync(ctx->flags.p, 0, sizeof(int) * kNumFlags, s));
-    CK(plan_batches(as<int64_t>(ctx->tile_word), as<int64_t>(ctx->tile_unit), as<int64_t>(ctx->tile_qoff), T,
-                    cap_words, as<int64_t>(ctx->boundaries), as<int64_t>(ctx->binfo), as<int64_t>(ctx->nb_d),
-                    as<int>(ctx->flags), s, &ctx->launches));
+    CK(plan_batches(as<int64_t>(ctx->tile_word) + tlo, as<int64_t>(ctx->tile_unit) + tlo,
+                    as<int64_t>(ctx->tile_qoff) + tlo, T, cap_words, as<int64_t>(ctx->boundaries),
+                    as<int64_t>(ctx->binfo), as<int64_t>(ctx->nb_d), as<int>(ctx->flags), s, &ctx->launches));
     int64_t nb = 0;
     int hflags[kNumFlags];
     CK(cudaMemcpyAsync(&nb, ctx->nb_d.p, 8, cudaMemcpyDeviceToHost, s));
@@ -567,8 +569,8 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
         ra.tile_word = as<int64_t>(ctx->tile_word);
         ra.tile_unit = as<int64_t>(ctx->tile_unit);
         ra.tile_qoff = as<int64_t>(ctx->tile_qoff);
-        ra.t0 = lo[3];
-        ra.t1 = hi[3];
+        ra.t0 = tlo + lo[3];
+        ra.t1 = tlo + hi[3];
         ra.unit0 = lo[1];
         ra.nunits = hi[1] - lo[1];
         ra.word0 = lo[0];
@@ -675,7 +677,7 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
     ctx->st.pairs = mode == HISS_OUT_CSR ? pairs : -1;
     ctx->st.batches = nb;
     ctx->st.query_tiles = T;
-    ctx->st.refine_units = ctx->total_units;
+    ctx->st.refine_units = info[4 * (size_t)nb + 1] - info[1];
     ctx->st.mask_words_max = max_words;
     ctx->st.ms_index = ms_index;
     ctx->st.ms_count = elapsed(ctx, 2, 3);
@@ -688,7 +690,9 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
 }
 
 
-int do_join(hiss_ctx *ctx, float eps, size_t batch_bytes, const hiss_out *out)
+// rank / nranks: run only the rank-th of nranks contiguous ranges of the
+// query tiles in processing order, balanced by refinement units.
+int do_join(hiss_ctx *ctx, float eps, size_t batch_bytes, const hiss_out *out, int32_t rank = 0, int32_t nranks = 1)
 {
     const int mode = out ? out->mode : HISS_OUT_CSR;
     if (mode != HISS_OUT_CSR && mode != HISS_OUT_MASK) return HISS_E_ARG;
@@ -703,7 +707,22 @@ int do_join(hiss_ctx *ctx, float eps, size_t batch_bytes, const hiss_out *out)
     ST(ensure_tiles(ctx, use_tc(ctx)));
     CK(cudaEventRecord(ctx->ev[3], s));
     fill_grid_stats(ctx);
-    return run_batches(ctx, self_side(ctx), eps, batch_bytes, out, ms_index, launches0);
+    int64_t tlo = 0, thi = ctx->T;
+    if (nranks > 1) {
+        // split points of the unit prefix sums: tile t belongs to the shard of its first unit
+        std::vector<int64_t> tu((size_t)ctx->T + 1);
+        CK(cudaMemcpyAsync(tu.data(), ctx->tile_unit.p, 8 * tu.size(), cudaMemcpyDeviceToHost, s));
+        ST(sync(ctx));
+        const int64_t U = tu[(size_t)ctx->T];
+        auto split = [&](int32_t r) -> int64_t {
+            if (r >= nranks) return ctx->T;
+            const int64_t target = (int64_t)((__int128)U * r / nranks);
+            return std::lower_bound(tu.begin(), tu.end() - 1, target) - tu.begin();
+        };
+        tlo = split(rank);
+        thi = split(rank + 1);
+    }
+    return run_batches(ctx, self_side(ctx), eps, batch_bytes, out, ms_index, launches0, tlo, thi);
 }
 
 // ---- semi-join: the query side built from separate query points -------------------
@@ -1254,6 +1273,16 @@ int hiss_gram_tf32(hiss_ctx *ctx, const float *d_a, const float *d_b, int32_t k,
     CK(gram_tf32(d_a, d_b, k, d_out, as<int>(ctx->flags), ctx->stream, &ctx->launches));
     ST(sync(ctx));
     return check_flags(ctx);
+}
+
+int hiss_join_shard(hiss_ctx *ctx, float eps, size_t batch_bytes, const hiss_out *out, int32_t rank,
+                    int32_t nranks)
+{
+    ST(enter(ctx));
+    if (!ctx->built) return HISS_E_STATE;
+    if (!(eps >= 0.0f) || std::isinf(eps)) return HISS_E_ARG;
+    if (nranks < 1 || rank < 0 || rank >= nranks) return HISS_E_ARG;
+    return do_join(ctx, eps, batch_bytes, out, rank, nranks);
 }
 
 int hiss_knn(hiss_ctx *ctx, int32_t k, float eps0, int64_t *d_ids, float *d_dist2)

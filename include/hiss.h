@@ -149,6 +149,18 @@ typedef struct {
  * cell's points in index order. */
 int hiss_join(hiss_ctx *ctx, float eps, size_t batch_bytes, const hiss_out *out);
 
+/* One shard of the self-join, for spreading one join over nranks GPUs (one
+ * context per GPU, each built from the same points: the index is
+ * deterministic, so every rank derives the same query tiles).  The query
+ * tiles in processing order are cut into nranks contiguous ranges with about
+ * equal refinement units (split at the unit prefix sums); this call runs
+ * range rank (0 <= rank < nranks) exactly as hiss_join runs all of them.
+ * Every query belongs to exactly one shard, so the union of the shards'
+ * batches is the join; no data moves between ranks.  RT-HiSS suggests
+ * offloading batches to other GPUs (Section VI); this is that split. */
+int hiss_join_shard(hiss_ctx *ctx, float eps, size_t batch_bytes, const hiss_out *out, int32_t rank,
+                    int32_t nranks);
+
 /* Semi-join (RT-HiSS Section II-A: "D and Q are distinct"; the method
  * applies unchanged): for each of nq query points (d_queries: device pointer,
  * nq x d float32 row-major, same d as the dataset, read only during the call)
