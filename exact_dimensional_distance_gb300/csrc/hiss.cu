@@ -69,6 +69,14 @@ struct hiss_ctx {
     void *h_pinned = nullptr;
     size_t h_cap = 0;
 
+    // overlapped host delivery (CSR to host): second set of batch outputs and
+    // pinned staging, a copy stream and its events (created on first use)
+    DBuf row_ptr2, cols2, query_ids2, query_rows2;
+    void *h_pinned2 = nullptr;
+    size_t h_cap2 = 0;
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t ev_compacted[2] = {}, ev_copy0[2] = {}, ev_copied[2] = {};
+
     // test helpers
     DBuf t_keys_alt, t_vals_alt, t_sort_tmp, t_scan_tmp;
 
@@ -474,18 +482,34 @@ int ensure_tiles(hiss_ctx *ctx, bool tc)
     return HISS_OK;
 }
 
-int ensure_pinned(hiss_ctx *ctx, size_t bytes)
+int ensure_pinned_slot(void *&ptr, size_t &cap, size_t bytes)
 {
-    if (ctx->h_cap >= bytes) return HISS_OK;
-    if (ctx->h_pinned) cudaFreeHost(ctx->h_pinned);
-    ctx->h_pinned = nullptr;
-    ctx->h_cap = 0;
-    cudaError_t e = cudaMallocHost(&ctx->h_pinned, bytes);
+    if (cap >= bytes) return HISS_OK;
+    if (ptr) cudaFreeHost(ptr);
+    ptr = nullptr;
+    cap = 0;
+    cudaError_t e = cudaMallocHost(&ptr, bytes);
     if (e != cudaSuccess) {
         cudaGetLastError();
+        ptr = nullptr;
         return HISS_E_NOMEM;
     }
-    ctx->h_cap = bytes;
+    cap = bytes;
+    return HISS_OK;
+}
+
+int ensure_pinned(hiss_ctx *ctx, size_t bytes) { return ensure_pinned_slot(ctx->h_pinned, ctx->h_cap, bytes); }
+
+// The copy stream and events of the overlapped host delivery.
+int ensure_copy_stream(hiss_ctx *ctx)
+{
+    if (ctx->copy_stream) return HISS_OK;
+    CK(cudaStreamCreateWithFlags(&ctx->copy_stream, cudaStreamNonBlocking));
+    for (int i = 0; i < 2; ++i) {
+        CK(cudaEventCreateWithFlags(&ctx->ev_compacted[i], cudaEventDisableTiming));
+        CK(cudaEventCreate(&ctx->ev_copy0[i]));
+        CK(cudaEventCreate(&ctx->ev_copied[i]));
+    }
     return HISS_OK;
 }
 
@@ -500,6 +524,9 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
     const int mode = out ? out->mode : HISS_OUT_CSR;
     const int to_host = out ? out->copy_to_host : 0;
     const bool tc = use_tc(ctx);  // the tiles were cut for this refinement
+    // CSR to host: batch b's copies run on the copy stream while batch b + 1
+    // is refined; outputs and pinned staging alternate between two slots
+    const bool ov = to_host && mode == HISS_OUT_CSR;
     hiss_batch_fn fn = out ? out->on_batch : nullptr;
     void *user = out ? out->user : nullptr;
     cudaStream_t s = ctx->stream;
@@ -544,6 +571,15 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
         ST(ensure(ctx, ctx->cand, 8 * (size_t)max_nq));
         ST(ensure(ctx, ctx->mask_row_ptr, 8 * (size_t)(max_nq + 1)));
     }
+    if (ov) {
+        ST(ensure_copy_stream(ctx));
+        ST(ensure(ctx, ctx->row_ptr2, 8 * (size_t)(max_nq + 1)));
+        ST(ensure(ctx, ctx->query_ids2, 8 * (size_t)max_nq));
+        ST(ensure(ctx, ctx->query_rows2, 4 * (size_t)max_nq));
+    }
+    int64_t pending = -1;  // overlapped delivery: batch whose copies are in flight
+    int pslot = 0;
+    hiss_batch pending_hb{};
 
     double ms_refine = 0.0, ms_compact = 0.0, ms_deliver = 0.0;
     int64_t pairs = 0;
@@ -551,6 +587,11 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
         const int64_t *lo = &info[4 * b], *hi = &info[4 * (b + 1)];
         const int64_t nq = hi[2] - lo[2];
         const int64_t nwords = hi[0] - lo[0];
+        const int slot = ov ? (int)(b & 1) : 0;
+        DBuf &rp_buf = slot ? ctx->row_ptr2 : ctx->row_ptr;
+        DBuf &cols_buf = slot ? ctx->cols2 : ctx->cols;
+        DBuf &qid_buf = slot ? ctx->query_ids2 : ctx->query_ids;
+        DBuf &qrow_buf = slot ? ctx->query_rows2 : ctx->query_rows;
         CK(cudaMemsetAsync(ctx->qcount.p, 0, 4 * (size_t)nq, s));
         // the refinement stores only nonzero mask words and marks them in occ;
         // the raw-mask output needs the zero words too
@@ -606,17 +647,17 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
         ca.nq = nq;
         ca.mask = ra.mask;
         ca.occ = ra.occ;
-        ca.query_ids = as<int64_t>(ctx->query_ids);
-        ca.query_rows = as<int32_t>(ctx->query_rows);
+        ca.query_ids = as<int64_t>(qid_buf);
+        ca.query_rows = as<int32_t>(qrow_buf);
         int64_t nnz = 0;
-        CK(scan_i32_to_i64(as<int32_t>(ctx->qcount), as<int64_t>(ctx->row_ptr), nq, as<int64_t>(ctx->scan_tmp), s,
+        CK(scan_i32_to_i64(as<int32_t>(ctx->qcount), as<int64_t>(rp_buf), nq, as<int64_t>(ctx->scan_tmp), s,
                            &ctx->launches));
-        CK(cudaMemcpyAsync(&nnz, as<int64_t>(ctx->row_ptr) + nq, 8, cudaMemcpyDeviceToHost, s));
+        CK(cudaMemcpyAsync(&nnz, as<int64_t>(rp_buf) + nq, 8, cudaMemcpyDeviceToHost, s));
         ST(sync(ctx));
         if (mode == HISS_OUT_CSR) {
-            ST(ensure(ctx, ctx->cols, 4 * (size_t)nnz));
-            ca.row_ptr = as<int64_t>(ctx->row_ptr);
-            ca.cols = as<int32_t>(ctx->cols);
+            ST(ensure(ctx, cols_buf, 4 * (size_t)nnz));
+            ca.row_ptr = as<int64_t>(rp_buf);
+            ca.cols = as<int32_t>(cols_buf);
         } else {
             ca.cand = as<int64_t>(ctx->cand);
             ca.mask_row_ptr = as<int64_t>(ctx->mask_row_ptr);
@@ -630,6 +671,49 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
         hb.nnz = nnz;
         hb.mode = mode;
         hb.n_words = mode == HISS_OUT_MASK ? nwords : 0;
+        if (ov) {
+            const size_t o_ids = 0, o_rp = align256(8 * nq), o_rows = o_rp + align256(8 * (nq + 1));
+            const size_t o_data = o_rows + align256(4 * nq);
+            const size_t bytes = o_data + 4 * (size_t)nnz + 256;
+            void *&hp = slot ? ctx->h_pinned2 : ctx->h_pinned;
+            size_t &hc = slot ? ctx->h_cap2 : ctx->h_cap;
+            ST(ensure_pinned_slot(hp, hc, bytes));
+            char *h = static_cast<char *>(hp);
+            cudaStream_t cs = ctx->copy_stream;
+            CK(cudaEventRecord(ctx->ev_compacted[slot], s));
+            CK(cudaStreamWaitEvent(cs, ctx->ev_compacted[slot], 0));
+            CK(cudaEventRecord(ctx->ev_copy0[slot], cs));
+            CK(cudaMemcpyAsync(h + o_ids, qid_buf.p, 8 * nq, cudaMemcpyDeviceToHost, cs));
+            CK(cudaMemcpyAsync(h + o_rows, qrow_buf.p, 4 * nq, cudaMemcpyDeviceToHost, cs));
+            CK(cudaMemcpyAsync(h + o_rp, rp_buf.p, 8 * (nq + 1), cudaMemcpyDeviceToHost, cs));
+            CK(cudaMemcpyAsync(h + o_data, cols_buf.p, 4 * (size_t)nnz, cudaMemcpyDeviceToHost, cs));
+            CK(cudaEventRecord(ctx->ev_copied[slot], cs));
+            hb.query_ids = reinterpret_cast<const int64_t *>(h + o_ids);
+            hb.row_ptr = reinterpret_cast<const int64_t *>(h + o_rp);
+            hb.query_rows = reinterpret_cast<const int32_t *>(h + o_rows);
+            hb.cols = reinterpret_cast<const int32_t *>(h + o_data);
+            hb.on_host = 1;
+            // hand over the previous batch, whose copies ran during this batch's refinement
+            if (pending >= 0) {
+                CK(cudaEventSynchronize(ctx->ev_copied[pslot]));
+                float cms = 0.0f;
+                if (cudaEventElapsedTime(&cms, ctx->ev_copy0[pslot], ctx->ev_copied[pslot]) == cudaSuccess)
+                    ms_deliver += cms;
+                cudaGetLastError();
+                if (fn && fn(user, &pending_hb) != 0) {
+                    cudaStreamSynchronize(cs);
+                    return HISS_E_CALLBACK;
+                }
+            }
+            ST(sync(ctx));
+            ms_refine += elapsed(ctx, 4, 5);
+            ms_compact += elapsed(ctx, 5, 6);
+            pairs += nnz;
+            pending = b;
+            pslot = slot;
+            pending_hb = hb;
+            continue;
+        }
         if (to_host) {
             const size_t o_ids = 0, o_rp = align256(8 * nq), o_rows = o_rp + align256(8 * (nq + 1));
             const size_t o_cand = o_rows + align256(4 * nq), o_data = o_cand + align256(8 * nq);
@@ -672,6 +756,13 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
         ms_deliver += elapsed(ctx, 6, 7);
         pairs += nnz;
         if (fn && fn(user, &hb) != 0) return HISS_E_CALLBACK;
+    }
+    if (pending >= 0) {
+        CK(cudaEventSynchronize(ctx->ev_copied[pslot]));
+        float cms = 0.0f;
+        if (cudaEventElapsedTime(&cms, ctx->ev_copy0[pslot], ctx->ev_copied[pslot]) == cudaSuccess) ms_deliver += cms;
+        cudaGetLastError();
+        if (fn && fn(user, &pending_hb) != 0) return HISS_E_CALLBACK;
     }
     ST(check_flags(ctx));
     ctx->st.pairs = mode == HISS_OUT_CSR ? pairs : -1;
@@ -1045,10 +1136,19 @@ void hiss_destroy(hiss_ctx *ctx)
                    &ctx->q_cell_of_row, &ctx->q_cell_start, &ctx->q_cell_key, &ctx->q_nbr, &ctx->q_nbr_cnt,
                    &ctx->q_bound, &ctx->q_work_key, &ctx->q_cell_idx, &ctx->q_work, &ctx->k_keys,
                    &ctx->k_vals, &ctx->k_keys_alt, &ctx->k_vals_alt, &ctx->k_sort_tmp, &ctx->k_d2, &ctx->k_prow,
-                   &ctx->k_done, &ctx->k_active};
+                   &ctx->k_done, &ctx->k_active, &ctx->row_ptr2, &ctx->cols2,
+                   &ctx->query_ids2, &ctx->query_rows2};
+    if (ctx->copy_stream) cudaStreamSynchronize(ctx->copy_stream);
     for (DBuf *b : all) release(ctx, *b);
     cudaStreamSynchronize(ctx->stream);
     if (ctx->h_pinned) cudaFreeHost(ctx->h_pinned);
+    if (ctx->h_pinned2) cudaFreeHost(ctx->h_pinned2);
+    for (int i = 0; i < 2; ++i) {
+        if (ctx->ev_compacted[i]) cudaEventDestroy(ctx->ev_compacted[i]);
+        if (ctx->ev_copy0[i]) cudaEventDestroy(ctx->ev_copy0[i]);
+        if (ctx->ev_copied[i]) cudaEventDestroy(ctx->ev_copied[i]);
+    }
+    if (ctx->copy_stream) cudaStreamDestroy(ctx->copy_stream);
     for (auto &e : ctx->ev)
         if (e) cudaEventDestroy(e);
     cudaGetLastError();
