@@ -52,9 +52,12 @@ struct Geo {
     static constexpr int TQ = kQueryWarps * 4 * MQ;  // queries per tile
     static constexpr int TP = kCandWarps * 8 * MP;   // candidates per staged tile
 };
-constexpr int kMaxStages = 4;
+#ifndef HISS_REFINE_STAGES
+#define HISS_REFINE_STAGES 6
+#endif
+constexpr int kMaxStages = HISS_REFINE_STAGES;
 
-// Stages of the candidate ring: as many as fit (up to 4, at least 2) in
+// Stages of the candidate ring: as many as fit (up to 6, at least 2) in
 // about a third of the SM's shared memory, so that two or three blocks stay
 // resident per SM.
 template <int MQ, int MP>
