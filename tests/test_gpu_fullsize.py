@@ -22,6 +22,15 @@ N_SAMPLE = 48
 
 @pytest.mark.parametrize("cfg", [2, 3, 4, 5])
 def test_full_size_sampled_rows(cfg):
+    _full_size(cfg, tensor=False)
+
+
+@pytest.mark.parametrize("cfg", [2, 4])
+def test_full_size_sampled_rows_tensor_cores(cfg):
+    _full_size(cfg, tensor=True)
+
+
+def _full_size(cfg, tensor):
     import __graft_entry__
     __graft_entry__.build()
     import exact_dimensional_distance_gb300 as edd
@@ -31,6 +40,7 @@ def test_full_size_sampled_rows(cfg):
     eps = golden_eps(cfg)
     sample = datagen.sample_queries(n, N_SAMPLE, seed=500 + cfg)
     j = edd.Join()
+    j.set_refine(tensor)
     j.build(torch.from_numpy(x).cuda())
     counts = j.count(eps)
     want_bound = oracle.count_bound(x, eps)

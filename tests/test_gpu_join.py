@@ -188,6 +188,57 @@ def test_device_and_host_delivery_agree():
         assert np.array_equal(dev[q], np.sort(host[q]))
 
 
+def test_overlapped_host_delivery_many_batches_and_callback_stop():
+    # CSR to host with many batches: copies of batch b overlap the refinement
+    # of batch b + 1 (two pinned slots); the rows must match device delivery,
+    # batches arrive in order, and a callback that stops the join leaves the
+    # context usable
+    edd = _edd()
+    x = datagen.generate(2, n=8000)
+    eps = oracle.pick_eps(x, 40, np.arange(0, 8000, 20))["eps"]
+    j = edd.Join()
+    j.build(torch.from_numpy(x).cuda())
+    host, order = {}, []
+
+    def take(b):
+        order.append(int(b.index))
+        q = edd._host_array(b.query_ids, b.nq, np.int64)
+        rp = edd._host_array(b.row_ptr, b.nq + 1, np.int64)
+        cols = edd._host_array(b.cols, b.nnz, np.int32)
+        assert b.on_host == 1
+        for i in range(b.nq):
+            host[int(q[i])] = np.sort(cols[rp[i]:rp[i + 1]])
+
+    st = j.join(eps, 1 << 16, edd.HISS_OUT_CSR, True, take)
+    assert st["batches"] >= 3 and order == list(range(st["batches"]))
+    dev = j.join_sets(eps)  # one batch
+    assert set(host) == set(dev) == set(range(len(x)))
+    for q in range(len(x)):
+        assert np.array_equal(host[q], np.sort(dev[q]))
+    calls = [0]
+
+    def stop(b):
+        calls[0] += 1
+        if calls[0] == 2:
+            raise RuntimeError("stop")
+
+    with pytest.raises(RuntimeError):
+        j.join(eps, 1 << 16, edd.HISS_OUT_CSR, True, stop)
+    again = j.join_sets(eps, 1 << 16)
+    assert all(np.array_equal(np.sort(again[q]), np.sort(dev[q])) for q in range(len(x)))
+    j.close()
+
+
+def test_refine_option_values():
+    edd = _edd()
+    import ctypes
+    j = edd.Join()
+    for v in (2, -1, 7):
+        assert edd.hiss_set_option(j.handle, edd.HISS_OPT_REFINE, v) == edd.HISS_E_ARG
+    assert edd.hiss_set_option(j.handle, 99, 0) == edd.HISS_E_ARG
+    j.close()
+
+
 def test_host_build_matches_device_build():
     edd = _edd()
     x = datagen.generate(4, n=2000)
