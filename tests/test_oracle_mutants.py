@@ -98,3 +98,51 @@ def test_mutant_is_caught(name, tmp_path):
     subprocess.check_call(["gcc", "-O1", "-fopenmp", "-ffp-contract=off", "-shared", "-fPIC",
                            "-o", str(so), str(c)])
     assert not _pins_hold(_load(str(so))), "pins did not catch mutant %s" % name
+
+
+# ---- kNN oracle: planted mistakes in copies of its Python definition ----------
+
+def _knn_variant(kind):
+    def knn(x, k, query_rows=None):
+        x64 = np.asarray(x, np.float32).astype(np.float64)
+        n = x64.shape[0]
+        q = np.arange(n) if query_rows is None else np.asarray(query_rows)
+        ids = np.empty((q.size, k), np.int64)
+        d2 = np.empty((q.size, k))
+        for r, i in enumerate(q.tolist()):
+            s = ((x64 - x64[i]) ** 2).sum(axis=1)
+            if kind == "abs_not_square":
+                s = np.abs(x64 - x64[i]).sum(axis=1)
+            if kind == "self_excluded":
+                s[i] = np.inf
+            tie = np.arange(n) if kind != "ties_by_higher_index" else -np.arange(n)
+            order = np.lexsort((tie, s))
+            if kind == "off_by_one":
+                order = order[1:]
+            order = order[:k]
+            ids[r] = order
+            d2[r] = s[order]
+        return ids, d2
+    return knn
+
+
+def _knn_pins(knn):
+    """The kNN pins of test_oracle.py, for a given implementation."""
+    x = np.array([[0], [1], [3], [6], [10]], np.float32)
+    ids, d2 = knn(x, 3)
+    assert ids.tolist() == [[0, 1, 2], [1, 0, 2], [2, 1, 0], [3, 2, 4], [4, 3, 2]]
+    assert d2.tolist() == [[0, 1, 9], [0, 1, 4], [0, 4, 9], [0, 9, 16], [0, 16, 49]]
+    rng = np.random.default_rng(11)
+    x = rng.integers(0, 4, size=(40, 3)).astype(np.float32)
+    ids, _ = knn(x, 7)
+    assert ids.tolist() == oracle.knn_py(x, 7)
+
+
+def test_knn_pins_hold_for_the_oracle():
+    _knn_pins(oracle.knn)
+
+
+@pytest.mark.parametrize("kind", ["self_excluded", "ties_by_higher_index", "off_by_one", "abs_not_square"])
+def test_knn_pins_catch_planted_mistakes(kind):
+    with pytest.raises(AssertionError):
+        _knn_pins(_knn_variant(kind))
