@@ -26,6 +26,7 @@ namespace {
 // Row stride of a staged candidate tile, in floats: d4 plus padding chosen so
 // that stride / 4 is odd, which makes the 8-byte loads of 8 consecutive rows
 // hit 8 distinct bank quads.
+
 __host__ __device__ __forceinline__ int tile_stride(int d4) { return ((d4 / 4) % 2 == 0) ? d4 + 4 : d4 + 8; }
 
 // Row stride of the pair-interleaved query tile, in floats: 2 d4 + 4, so that
@@ -170,16 +171,50 @@ __device__ __forceinline__ float min3(float a, float b, float c)
     return r;
 }
 
-// Smallest of the thread's MQ x MP partial sums (three-input minima).
+// One level of a min tree over v[0..N): v[t] = min(v[3t], v[3t+1], v[3t+2]),
+// repeated until one value is left (indices are compile-time constants, so v
+// stays in registers).
+template <int N>
+__device__ __forceinline__ void min_levels(float (&v)[32])
+{
+    constexpr int M = (N + 2) / 3;
+#pragma unroll
+    for (int t = 0; t < M; ++t) {
+        const int b = 3 * t;
+        if (b + 2 < N) v[t] = min3(v[b], v[b + 1], v[b + 2]);
+        else if (b + 1 < N) v[t] = fminf(v[b], v[b + 1]);
+        else v[t] = v[b];
+    }
+    if constexpr (M > 1) min_levels<M>(v);
+}
+
+// Smallest of the thread's MQ x MP partial sums: a tree of three-input
+// minima (depth 4 for 32 values instead of a chain of 16 dependent ones).
 template <int MQ, int MP>
 __device__ __forceinline__ float block_min(const f32x2 (&acc)[MQ / 2][MP])
 {
-    float m = lo_of(acc[0][0]);
+    constexpr int N = MQ * MP;
+    static_assert(N <= 32, "min tree size");
+    float v[32];
 #pragma unroll
     for (int i2 = 0; i2 < MQ / 2; ++i2)
 #pragma unroll
-        for (int j = 0; j < MP; ++j) m = min3(m, lo_of(acc[i2][j]), hi_of(acc[i2][j]));
-    return m;
+        for (int j = 0; j < MP; ++j) {
+            v[2 * (i2 * MP + j)] = lo_of(acc[i2][j]);
+            v[2 * (i2 * MP + j) + 1] = hi_of(acc[i2][j]);
+        }
+    min_levels<N>(v);
+    return v[0];
+}
+
+// Where a warp checks for early termination (k = dimensions summed so far):
+// with 8 x 4 blocks (d4 <= 64) after every 2 dimensions, with 4 x 4 blocks
+// after every 4 (there the pairs leave later, and the shorter steps need two
+// per loop iteration to overlap their loads).
+template <int MQ>
+__device__ __forceinline__ bool exit_check_at(int k)
+{
+    return MQ == 8 || (k & 3) == 0;
 }
 
 // Resident blocks per SM the register budget is sized for.
@@ -335,48 +370,67 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
         const float *P = P0 + st * kTP * S;
         f32x2 acc[MQ / 2][MP];
         if constexpr (PROF) {
-            // all dimensions, counting live pairs step by step
+            // all dimensions, counting live pairs step by step: the
+            // method's per-pair exit every 4 dimensions (prof_alg) and the
+            // warp schedule of the kernel below (prof_exec)
             bool warp_live = true;
             block_step2<MQ, MP, true>(acc, Q2, P, S2, S, pidbase, pbase, 0);
-            block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, 2);
             int valid = 0;
 #pragma unroll
             for (int i = 0; i < MQ; ++i)
 #pragma unroll
                 for (int j = 0; j < MP; ++j) valid += (qbase + 4 * i < nq && v0 + pbase + 8 * j < vend) ? 1 : 0;
             prof_alg += (uint64_t)valid * (uint64_t)min(4, a.d);
-            prof_exec += (uint64_t)valid * (uint64_t)min(4, a.d);
-            for (int k = 4; k < d4; k += 4) {
-                int live = 0;
+            prof_exec += (uint64_t)valid * (uint64_t)min(2, a.d);
+            for (int k = 2; k < d4; k += 2) {
+                if (warp_live && exit_check_at<MQ>(k) && __all_sync(0xffffffffu, block_min<MQ, MP>(acc) > eps2))
+                    warp_live = false;
+                if ((k & 3) == 0) {
+                    int live = 0;
 #pragma unroll
-                for (int i = 0; i < MQ; ++i)
+                    for (int i = 0; i < MQ; ++i)
 #pragma unroll
-                    for (int j = 0; j < MP; ++j) live += (acc_at<MQ, MP>(acc, i, j) <= eps2) ? 1 : 0;
-                if (__all_sync(0xffffffffu, block_min<MQ, MP>(acc) > eps2)) warp_live = false;
-                if (!__any_sync(0xffffffffu, live > 0) && !warp_live) break;
-                const uint64_t step = (uint64_t)min(4, a.d - k);
-                prof_alg += (uint64_t)live * step;
-                if (warp_live) prof_exec += (uint64_t)valid * step;
+                        for (int j = 0; j < MP; ++j) live += (acc_at<MQ, MP>(acc, i, j) <= eps2) ? 1 : 0;
+                    if (!__any_sync(0xffffffffu, live > 0) && !warp_live) break;
+                    prof_alg += (uint64_t)live * (uint64_t)min(4, a.d - k);
+                }
+                if (warp_live) prof_exec += (uint64_t)valid * (uint64_t)max(0, min(2, a.d - k));
                 block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k);
-                block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k + 2);
             }
         } else {
             block_step2<MQ, MP, true>(acc, Q2, P, S2, S, pidbase, pbase, 0);
-            block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, 2);
             // warp-level early termination (the pairs are in variance order,
             // most leave early)
             bool any_close = true;
-            for (int k = 4;; k += 4) {
-                if (k == d4) {
-                    any_close = __any_sync(0xffffffffu, block_min<MQ, MP>(acc) <= eps2);
-                    break;
+            if constexpr (MQ == 8) {
+                // a check after every 2 dimensions
+                for (int k = 2;; k += 2) {
+                    if (k == d4) {
+                        any_close = __any_sync(0xffffffffu, block_min<MQ, MP>(acc) <= eps2);
+                        break;
+                    }
+                    if (exit_check_at<MQ>(k) && __all_sync(0xffffffffu, block_min<MQ, MP>(acc) > eps2)) {
+                        any_close = false;
+                        break;
+                    }
+                    block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k);
                 }
-                if (__all_sync(0xffffffffu, block_min<MQ, MP>(acc) > eps2)) {
-                    any_close = false;
-                    break;
+            } else {
+                // a check after every 4 dimensions; two steps per iteration
+                // let the compiler overlap one step's loads with the other
+                block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, 2);
+                for (int k = 4;; k += 4) {
+                    if (k == d4) {
+                        any_close = __any_sync(0xffffffffu, block_min<MQ, MP>(acc) <= eps2);
+                        break;
+                    }
+                    if (__all_sync(0xffffffffu, block_min<MQ, MP>(acc) > eps2)) {
+                        any_close = false;
+                        break;
+                    }
+                    block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k);
+                    block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k + 2);
                 }
-                block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k);
-                block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k + 2);
             }
             // one bit per pair.  The warp's 32 candidate columns (pbase + 8 j)
             // form one mask word per query row: bit lp + 8 j.  A ballot per

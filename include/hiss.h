@@ -275,8 +275,9 @@ int hiss_set_option(hiss_ctx *ctx, int option, int64_t value);
  * sum exceeds eps^2 (capped at d) -- the method's minimal refinement work
  * with early termination (RT-HiSS Section IV-A); out[1] = the dimensions
  * hiss_join's refinement kernel actually evaluates, whose warps abandon a
- * block of pairs only when all of them exceed eps^2 (checked after every 4
- * dimensions).  out is a host int64[2].  Costs about one
+ * block of pairs only when all of them exceed eps^2 (checked after every 2
+ * dimensions up to d4 = 64, every 4 above).  out is a host int64[2].  Costs
+ * about one
  * join's refinement with no early termination. */
 int hiss_work_profile(hiss_ctx *ctx, float eps, int64_t *out);
 
