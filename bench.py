@@ -232,6 +232,9 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=8000)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-batch-bytes", type=int, default=None,
+                    help="result-mask bytes per batch of the end-to-end leg (default: --batch-bytes); with "
+                         "several batches one batch's copies to host overlap the next batch's refinement")
     ap.add_argument("--n", type=int, default=None,
                     help="draw a smaller instance of the workload (profiling only; not the benchmark workload)")
     args = ap.parse_args()
@@ -345,6 +348,8 @@ def main():
 
     if not args.no_e2e:
         # end to end through the host-buffer entry points
+        if args.e2e_batch_bytes is None:
+            args.e2e_batch_bytes = args.batch_bytes
         hx_t = torch.from_numpy(x).pin_memory()
         hx = hx_t.numpy()
         d2h = [0]
@@ -356,9 +361,9 @@ def main():
             j.build(hx)
             j.count(eps, out=False)
             if args.shard:
-                j.join_shard(eps, rank, world, args.batch_bytes, edd.HISS_OUT_CSR, True, on_batch)
+                j.join_shard(eps, rank, world, args.e2e_batch_bytes, edd.HISS_OUT_CSR, True, on_batch)
             else:
-                j.join(eps, args.batch_bytes, edd.HISS_OUT_CSR, True, on_batch)
+                j.join(eps, args.e2e_batch_bytes, edd.HISS_OUT_CSR, True, on_batch)
 
         e2e_step()
         torch.cuda.synchronize()
@@ -372,7 +377,8 @@ def main():
         te, e2e_units = aggregate(time.perf_counter() - t0, pairs * args.steps, dist, torch.device("cuda", local))
         line["e2e"] = {"value": e2e_units / te, "unit": UNIT,
                        "h2d_bytes_per_step": int(x.nbytes), "d2h_bytes_per_step": int(d2h[0] // args.steps),
-                       "ms_per_step": 1e3 * te / args.steps}
+                       "ms_per_step": 1e3 * te / args.steps, "batch_bytes": args.e2e_batch_bytes,
+                       "batches": j.stats()["batches"]}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args, x, eps)

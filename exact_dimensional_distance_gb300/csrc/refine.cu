@@ -11,11 +11,13 @@
 // distances (4 x 4 above 64 dimensions), held as packed float32 pairs, and
 // adds two dimensions per step with f32x2 subtract / multiply-add
 // instructions (one instruction per pair and dimension instead of two).
-// Dimensions are in variance order, so after every 4 dimensions a warp checks
-// whether all of its partial sums already exceed eps^2 and, if so, leaves the
-// tile (early termination, Section IV-A).  The result is one bit per pair, sum <= eps^2,
-// written to the query's mask row; the popcount of each word is accumulated
-// into the query's neighbour count.
+// Dimensions are in variance order, so after every 2 dimensions (8 x 4
+// blocks) or 4 (4 x 4 blocks) a warp checks whether all of its partial sums
+// already exceed eps^2 and, if so, leaves the tile (early termination,
+// Section IV-A); with 4 x 4 blocks a warp left with few pairs within eps^2
+// after 64 dimensions finishes them one pair per lane.  The result is one
+// bit per pair, sum <= eps^2, written to the query's mask row; the popcount
+// of each word is accumulated into the query's neighbour count.
 #include "hiss_internal.cuh"
 #include "ptx.cuh"
 
@@ -68,12 +70,32 @@ __host__ __device__ __forceinline__ int refine_stages(int d4)
     int ns = (75 * 1024 - q2) / stage;
     return ns < 2 ? 2 : (ns > kMaxStages ? kMaxStages : ns);
 }
+// Survivor mode (4 x 4 blocks, d4 > 64 only).  A warp still in a tile after
+// kSurvDim dimensions counts its pairs whose partial sum is still <= eps^2;
+// if there are at most kSurvMax of them and at least 8 dimensions are left,
+// it stops the blocked arithmetic and finishes those pairs one per lane,
+// continuing each pair's own float32 sum in dimension order (the same
+// subtract and multiply-add, so the same sums and bits), with a per-pair exit
+// every 4 dimensions.  With 8 x 4 blocks (d4 <= 64) the lists cost a ring
+// stage and registers for less than they save, so that shape has no
+// survivor mode.
+constexpr int kSurvDim = 64;  // a multiple of 4
+constexpr int kSurvMax = 64;  // survivors a warp takes (a multiple of 32)
+template <int MQ>
+__host__ __device__ __forceinline__ constexpr size_t surv_bytes()
+{
+    // per compute warp: kSurvMax partial sums (float) and pair codes (uint16),
+    // and 32 mask words
+    return MQ == 4 ? (size_t)kComputeWarps * (kSurvMax * 6 + 32 * 4) : 0;
+}
+
 template <int MQ, int MP>
 __host__ __forceinline__ size_t refine_smem(int d4)
 {
     using G = Geo<MQ, MP>;
     return sizeof(float) *
-           ((size_t)(G::TQ / 2) * pair_stride(d4) + (size_t)refine_stages<MQ, MP>(d4) * G::TP * tile_stride(d4));
+               ((size_t)(G::TQ / 2) * pair_stride(d4) + (size_t)refine_stages<MQ, MP>(d4) * G::TP * tile_stride(d4)) +
+           surv_bytes<MQ>();
 }
 
 // Packed float32 pairs (two lanes of one 64-bit register), computed with the
@@ -207,6 +229,67 @@ __device__ __forceinline__ float block_min(const f32x2 (&acc)[MQ / 2][MP])
     return v[0];
 }
 
+// Survivor mode of one warp at dimension k: the pairs of its MQ x MP blocks
+// whose partial sum is still <= eps^2 (at most kSurvMax over the warp) are
+// listed in shared memory (query row << 5 | candidate column within the warp
+// tile, and the partial sum), then finished one per lane: dimensions k, k+1,
+// ... are added to the pair's own partial sum with the blocked path's
+// round-to-nearest subtract and fused multiply-add, in the same order, so the
+// final sum and bit are those of the blocked path.  A pair stops once its sum
+// exceeds eps^2 (checked every 4 dimensions).  The bits of the pairs within
+// eps^2 are gathered in sword[query row of the warp tile] (bit = candidate
+// column), ready for the caller after the closing __syncwarp.
+template <int MQ, int MP>
+__device__ __forceinline__ void survivors(const f32x2 (&acc)[MQ / 2][MP], const float *Q2, const float *P, int S2,
+                                          int S, int k, int d4, float eps2, int first, int total, int lane, int wq,
+                                          int wp, float *spart, uint16_t *sidx, uint32_t *sword)
+{
+    const int lq = lane >> 3, lp = lane & 7;
+    int pos = first;
+#pragma unroll
+    for (int i = 0; i < MQ; ++i)
+#pragma unroll
+        for (int j = 0; j < MP; ++j) {
+            const float v = acc_at<MQ, MP>(acc, i, j);
+            if (v <= eps2) {
+                sidx[pos] = (uint16_t)(((lq + 4 * i) << 5) | (lp + 8 * j));
+                spart[pos] = v;
+                ++pos;
+            }
+        }
+    sword[lane] = 0u;
+    __syncwarp();
+    for (int e0 = 0; e0 < total; e0 += 32) {
+        const int e = e0 + lane;
+        if (e < total) {
+            const int code = sidx[e];
+            const int r = code >> 5, pc = code & 31;
+            const int qt = wq * (4 * MQ) + r;  // query row of the tile
+            const float *qrow = Q2 + (4 * (qt >> 3) + (qt & 3)) * S2;
+            const bool hi = ((qt >> 2) & 1) != 0;  // second row of its pair row
+            const float *prow = P + (wp * (8 * MP) + pc) * S;
+            float sum = spart[e];
+            for (int kk = k; kk < d4; kk += 4) {
+                const float4 qa = *reinterpret_cast<const float4 *>(qrow + 2 * kk);
+                const float4 qb = *reinterpret_cast<const float4 *>(qrow + 2 * kk + 4);
+                const float4 pv = *reinterpret_cast<const float4 *>(prow + kk);
+                float df;
+                df = __fsub_rn(hi ? qa.y : qa.x, pv.x);
+                sum = __fmaf_rn(df, df, sum);
+                df = __fsub_rn(hi ? qa.w : qa.z, pv.y);
+                sum = __fmaf_rn(df, df, sum);
+                df = __fsub_rn(hi ? qb.y : qb.x, pv.z);
+                sum = __fmaf_rn(df, df, sum);
+                df = __fsub_rn(hi ? qb.w : qb.z, pv.w);
+                sum = __fmaf_rn(df, df, sum);
+                if (sum > eps2) break;
+            }
+            if (sum <= eps2) atomicOr(&sword[r], 1u << pc);
+        }
+    }
+    __syncwarp();
+}
+
 // Where a warp checks for early termination (k = dimensions summed so far):
 // with 8 x 4 blocks (d4 <= 64) after every 2 dimensions, with 4 x 4 blocks
 // after every 4 (there the pairs leave later, and the shorter steps need two
@@ -237,7 +320,11 @@ __device__ __forceinline__ bool exit_check_at(int k)
 // dimensions a pair needs when it stops at the first multiple of 4 whose
 // partial sum exceeds eps^2 (prof[0]), and the dimensions the warp-level
 // schedule of the PROF = false kernel executes (prof[1]).
-template <int MQ, int MP, bool PROF>
+//
+// D4 > 0: the kernel is compiled for that padded dimension (equal to a.d4),
+// so every shared-memory row offset is an immediate and the dimension loop
+// has a constant trip count; D4 = 0 takes a.d4 at run time.
+template <int MQ, int MP, bool PROF, int D4>
 __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(const RefineArgs a)
 {
     constexpr int kTQ = Geo<MQ, MP>::TQ, kTP = Geo<MQ, MP>::TP;
@@ -249,10 +336,14 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
     __shared__ int64_t s_info[2];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int d4 = a.d4, S = tile_stride(d4), S2 = pair_stride(d4), C4 = d4 / 4;
+    const int d4 = D4 > 0 ? D4 : a.d4, S = tile_stride(d4), S2 = pair_stride(d4), C4 = d4 / 4;
     const int nst = refine_stages<MQ, MP>(d4);
     float *Q2 = smem;
     float *P0 = smem + (kTQ / 2) * S2;
+    // survivor lists (MQ == 4) after the stage ring
+    float *s_spart = P0 + nst * kTP * S;
+    uint16_t *s_sidx = reinterpret_cast<uint16_t *>(s_spart + kComputeWarps * kSurvMax);
+    uint32_t *s_sword = reinterpret_cast<uint32_t *>(s_sidx + kComputeWarps * kSurvMax);
 
     if (tid == 0) {
         const int64_t u = a.unit0 + blockIdx.x;
@@ -373,7 +464,7 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
             // all dimensions, counting live pairs step by step: the
             // method's per-pair exit every 4 dimensions (prof_alg) and the
             // warp schedule of the kernel below (prof_exec)
-            bool warp_live = true;
+            bool warp_live = true, surv = false;
             block_step2<MQ, MP, true>(acc, Q2, P, S2, S, pidbase, pbase, 0);
             int valid = 0;
 #pragma unroll
@@ -382,26 +473,32 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
                 for (int j = 0; j < MP; ++j) valid += (qbase + 4 * i < nq && v0 + pbase + 8 * j < vend) ? 1 : 0;
             prof_alg += (uint64_t)valid * (uint64_t)min(4, a.d);
             prof_exec += (uint64_t)valid * (uint64_t)min(2, a.d);
+            int live = 0;
             for (int k = 2; k < d4; k += 2) {
-                if (warp_live && exit_check_at<MQ>(k) && __all_sync(0xffffffffu, block_min<MQ, MP>(acc) > eps2))
+                if (warp_live && !surv && exit_check_at<MQ>(k) &&
+                    __all_sync(0xffffffffu, block_min<MQ, MP>(acc) > eps2))
                     warp_live = false;
                 if ((k & 3) == 0) {
-                    int live = 0;
+                    live = 0;
 #pragma unroll
                     for (int i = 0; i < MQ; ++i)
 #pragma unroll
                         for (int j = 0; j < MP; ++j) live += (acc_at<MQ, MP>(acc, i, j) <= eps2) ? 1 : 0;
-                    if (!__any_sync(0xffffffffu, live > 0) && !warp_live) break;
+                    if (MQ == 4 && warp_live && !surv && k == kSurvDim && d4 - k >= 8 &&
+                        __reduce_add_sync(0xffffffffu, live) <= kSurvMax)
+                        surv = true;  // survivor mode: each live pair runs on alone
+                    if (!__any_sync(0xffffffffu, live > 0) && (!warp_live || surv)) break;
                     prof_alg += (uint64_t)live * (uint64_t)min(4, a.d - k);
                 }
-                if (warp_live) prof_exec += (uint64_t)valid * (uint64_t)max(0, min(2, a.d - k));
+                if (surv) prof_exec += (uint64_t)live * (uint64_t)max(0, min(2, a.d - k));
+                else if (warp_live) prof_exec += (uint64_t)valid * (uint64_t)max(0, min(2, a.d - k));
                 block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k);
             }
         } else {
             block_step2<MQ, MP, true>(acc, Q2, P, S2, S, pidbase, pbase, 0);
             // warp-level early termination (the pairs are in variance order,
             // most leave early)
-            bool any_close = true;
+            bool any_close = true, surv = false;
             if constexpr (MQ == 8) {
                 // a check after every 2 dimensions
                 for (int k = 2;; k += 2) {
@@ -428,6 +525,27 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
                         any_close = false;
                         break;
                     }
+                    if (k == kSurvDim && d4 - k >= 8) {
+                        int live = 0;
+#pragma unroll
+                        for (int i = 0; i < MQ; ++i)
+#pragma unroll
+                            for (int j = 0; j < MP; ++j) live += (acc_at<MQ, MP>(acc, i, j) <= eps2) ? 1 : 0;
+                        int incl = live;
+#pragma unroll
+                        for (int o = 1; o < 32; o <<= 1) {
+                            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                            if (lane >= o) incl += v;
+                        }
+                        const int total = __shfl_sync(0xffffffffu, incl, 31);
+                        if (total <= kSurvMax) {
+                            surv = true;
+                            survivors<MQ, MP>(acc, Q2, P, S2, S, k, d4, eps2, incl - live, total, lane, wq, wp,
+                                              s_spart + warp * kSurvMax, s_sidx + warp * kSurvMax,
+                                              s_sword + warp * 32);
+                            break;
+                        }
+                    }
                     block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k);
                     block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k + 2);
                 }
@@ -443,6 +561,9 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
             if (any_close) {
                 const uint32_t sel = (uint32_t)lq | ((uint32_t)(lq + 4) << 4);
                 uint32_t mine = 0;
+                if (surv) {
+                    if (lp < MQ) mine = s_sword[warp * 32 + lq + 4 * lp];
+                } else {
 #pragma unroll
                 for (int i = 0; i < MQ; ++i) {
                     uint32_t bj[MP];
@@ -451,6 +572,7 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
                     const uint32_t w01 = __byte_perm(bj[0], bj[1], sel), w23 = __byte_perm(bj[2], bj[3], sel);
                     const uint32_t w = __byte_perm(w01, w23, 0x5410);
                     if (lp == i) mine = w;
+                }
                 }
                 if (lp < MQ && qr < nq && wcol < W && mine) {
                     // only nonzero words are stored; the occupancy bitmap marks them
@@ -482,17 +604,18 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
     }
 }
 
-template <int MQ, int MP, bool PROF>
+template <int MQ, int MP, bool PROF, int D4 = 0>
 cudaError_t launch_refine(const RefineArgs &a, cudaStream_t s)
 {
     const size_t smem = refine_smem<MQ, MP>(a.d4);
     static size_t configured = 0;  // largest dynamic shared memory requested so far
     if (smem > configured) {
-        HISS_TRY(cudaFuncSetAttribute(k_refine<MQ, MP, PROF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        HISS_TRY(cudaFuncSetAttribute(k_refine<MQ, MP, PROF, D4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)smem));
         configured = smem;
     }
     if (a.nunits <= 0) return cudaSuccess;
-    k_refine<MQ, MP, PROF><<<(unsigned)a.nunits, kRefineThreads, smem, s>>>(a);
+    k_refine<MQ, MP, PROF, D4><<<(unsigned)a.nunits, kRefineThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -622,9 +745,23 @@ __global__ void k_word_positions(const uint32_t *words, int64_t nbits, const int
 
 int refine_tq(int d4) { return d4 <= 64 ? Geo<8, 4>::TQ : Geo<4, 4>::TQ; }
 
+#ifndef HISS_REFINE_SPECIALIZE
+#define HISS_REFINE_SPECIALIZE 1
+#endif
+
 cudaError_t refine(const RefineArgs &a, cudaStream_t s, int64_t *launches)
 {
     ++*launches;
+#if HISS_REFINE_SPECIALIZE
+    // the padded dimensions of the common workloads get their own builds
+    switch (a.d4) {
+        case 16: return launch_refine<8, 4, false, 16>(a, s);
+        case 32: return launch_refine<8, 4, false, 32>(a, s);
+        case 64: return launch_refine<8, 4, false, 64>(a, s);
+        case 128: return launch_refine<4, 4, false, 128>(a, s);
+        default: break;
+    }
+#endif
     return a.d4 <= 64 ? launch_refine<8, 4, false>(a, s) : launch_refine<4, 4, false>(a, s);
 }
 
