@@ -14,8 +14,8 @@
 // Dimensions are in variance order, so after every 2 dimensions (8 x 4
 // blocks) or 4 (4 x 4 blocks) a warp checks whether all of its partial sums
 // already exceed eps^2 and, if so, leaves the tile (early termination,
-// Section IV-A); with 4 x 4 blocks a warp left with few pairs within eps^2
-// after 64 dimensions finishes them one pair per lane.  The result is one
+// Section IV-A); at 64 dimensions and more, a warp left with few pairs
+// within eps^2 finishes them one pair per lane.  The result is one
 // bit per pair, sum <= eps^2, written to the query's mask row; the popcount
 // of each word is accumulated into the query's neighbour count.
 #include "hiss_internal.cuh"
@@ -70,23 +70,36 @@ __host__ __device__ __forceinline__ int refine_stages(int d4)
     int ns = (75 * 1024 - q2) / stage;
     return ns < 2 ? 2 : (ns > kMaxStages ? kMaxStages : ns);
 }
-// Survivor mode (4 x 4 blocks, d4 > 64 only).  A warp still in a tile after
-// kSurvDim dimensions counts its pairs whose partial sum is still <= eps^2;
-// if there are at most kSurvMax of them and at least 8 dimensions are left,
-// it stops the blocked arithmetic and finishes those pairs one per lane,
-// continuing each pair's own float32 sum in dimension order (the same
-// subtract and multiply-add, so the same sums and bits), with a per-pair exit
-// every 4 dimensions.  With 8 x 4 blocks (d4 <= 64) the lists cost a ring
-// stage and registers for less than they save, so that shape has no
-// survivor mode.
-constexpr int kSurvDim = 64;  // a multiple of 4
+// Survivor mode.  A warp still in a tile after surv_dim dimensions counts its
+// pairs whose partial sum is still <= eps^2; if there are at most kSurvMax
+// of them and at least 8 dimensions are left, it stops the blocked
+// arithmetic and finishes those pairs one per lane, continuing each pair's
+// own float32 sum in dimension order (the same subtract and multiply-add, so
+// the same sums and bits), with a per-pair exit every 4 dimensions.  It is
+// used with 4 x 4 blocks (d4 > 64) and with 8 x 4 blocks at d4 = 64.  With
+// fewer dimensions the one-pair-per-lane path (2 scalar instructions and
+// about 0.75 shared loads per pair-dimension, against 1 packed instruction in
+// a register block) costs more than the blocked dimensions it saves.  The
+// lists sit in dynamic shared memory after the ring, only in builds that use
+// them.
+#ifndef HISS_SURV8_DIM
+#define HISS_SURV8_DIM 16
+#endif
+#ifndef HISS_SURV4_DIM
+#define HISS_SURV4_DIM 48
+#endif
 constexpr int kSurvMax = 64;  // survivors a warp takes (a multiple of 32)
-template <int MQ>
-__host__ __device__ __forceinline__ constexpr size_t surv_bytes()
+// Dimension after which a warp may switch to survivor mode (a multiple of 4),
+// 0 for none.
+__host__ __device__ __forceinline__ constexpr int surv_dim(int mq, int d4)
+{
+    return mq == 4 ? HISS_SURV4_DIM : (d4 == 64 ? HISS_SURV8_DIM : 0);
+}
+__host__ __device__ __forceinline__ constexpr size_t surv_bytes(int mq, int d4)
 {
     // per compute warp: kSurvMax partial sums (float) and pair codes (uint16),
     // and 32 mask words
-    return MQ == 4 ? (size_t)kComputeWarps * (kSurvMax * 6 + 32 * 4) : 0;
+    return surv_dim(mq, d4) > 0 ? (size_t)kComputeWarps * (kSurvMax * 6 + 32 * 4) : 0;
 }
 
 template <int MQ, int MP>
@@ -95,7 +108,7 @@ __host__ __forceinline__ size_t refine_smem(int d4)
     using G = Geo<MQ, MP>;
     return sizeof(float) *
                ((size_t)(G::TQ / 2) * pair_stride(d4) + (size_t)refine_stages<MQ, MP>(d4) * G::TP * tile_stride(d4)) +
-           surv_bytes<MQ>();
+           surv_bytes(MQ, d4);
 }
 
 // Packed float32 pairs (two lanes of one 64-bit register), computed with the
@@ -484,7 +497,7 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
                     for (int i = 0; i < MQ; ++i)
 #pragma unroll
                         for (int j = 0; j < MP; ++j) live += (acc_at<MQ, MP>(acc, i, j) <= eps2) ? 1 : 0;
-                    if (MQ == 4 && warp_live && !surv && k == kSurvDim && d4 - k >= 8 &&
+                    if (warp_live && !surv && k == surv_dim(MQ, d4) && d4 - k >= 8 &&
                         __reduce_add_sync(0xffffffffu, live) <= kSurvMax)
                         surv = true;  // survivor mode: each live pair runs on alone
                     if (!__any_sync(0xffffffffu, live > 0) && (!warp_live || surv)) break;
@@ -510,6 +523,27 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
                         any_close = false;
                         break;
                     }
+                    if (k == surv_dim(MQ, d4) && d4 - k >= 8) {
+                        int live = 0;
+#pragma unroll
+                        for (int i = 0; i < MQ; ++i)
+#pragma unroll
+                            for (int j = 0; j < MP; ++j) live += (acc_at<MQ, MP>(acc, i, j) <= eps2) ? 1 : 0;
+                        int incl = live;
+#pragma unroll
+                        for (int o = 1; o < 32; o <<= 1) {
+                            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                            if (lane >= o) incl += v;
+                        }
+                        const int total = __shfl_sync(0xffffffffu, incl, 31);
+                        if (total <= kSurvMax) {
+                            surv = true;
+                            survivors<MQ, MP>(acc, Q2, P, S2, S, k, d4, eps2, incl - live, total, lane, wq, wp,
+                                              s_spart + warp * kSurvMax, s_sidx + warp * kSurvMax,
+                                              s_sword + warp * 32);
+                            break;
+                        }
+                    }
                     block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k);
                 }
             } else {
@@ -525,7 +559,7 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
                         any_close = false;
                         break;
                     }
-                    if (k == kSurvDim && d4 - k >= 8) {
+                    if (k == surv_dim(MQ, d4) && d4 - k >= 8) {
                         int live = 0;
 #pragma unroll
                         for (int i = 0; i < MQ; ++i)
@@ -698,15 +732,19 @@ __global__ void __launch_bounds__(kCompactWarps * 32) k_compact(const CompactArg
         for (uint32_t bb = bits; bb; bb &= bb - 1) {
             const int64_t w = 32 * o + __ffs(bb) - 1;
             uint32_t word = a.mask[w];
+            // stencil slot of the word's first candidate (binary search),
+            // then forward: the bits are visited in increasing order
+            const int64_t v0 = (w - woff) * 32;
+            int l = 0, hh = ns - 1;
+            while (l < hh) {
+                const int m = (l + hh + 1) >> 1;
+                if (s_vpre[warp][m] <= v0) l = m; else hh = m - 1;
+            }
             while (word) {
                 const int b = __ffs(word) - 1;
                 word &= word - 1;
-                const int64_t v = (w - woff) * 32 + b;
-                int l = 0, hh = ns - 1;
-                while (l < hh) {
-                    const int m = (l + hh + 1) >> 1;
-                    if (s_vpre[warp][m] <= v) l = m; else hh = m - 1;
-                }
+                const int64_t v = v0 + b;
+                while (l + 1 < ns && s_vpre[warp][l + 1] <= v) ++l;
                 out[pos++] = a.ids[s_start[warp][l] + (v - s_vpre[warp][l])];
             }
         }
