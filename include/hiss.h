@@ -276,8 +276,10 @@ int hiss_set_option(hiss_ctx *ctx, int option, int64_t value);
  * with early termination (RT-HiSS Section IV-A); out[1] = the dimensions
  * hiss_join's refinement kernel actually evaluates, whose warps abandon a
  * block of pairs only when all of them exceed eps^2 (checked after every 2
- * dimensions up to d4 = 64, every 4 above).  out is a host int64[2].  Costs
- * about one
+ * dimensions up to d4 = 64, every 4 above); from d4 = 64 on, a warp left
+ * with at most 64 pairs within eps^2 after 16 (d4 = 64) or 48 (d4 > 64)
+ * dimensions finishes those pairs alone, each stopping when it exceeds
+ * eps^2.  out is a host int64[2].  Costs about one
  * join's refinement with no early termination. */
 int hiss_work_profile(hiss_ctx *ctx, float eps, int64_t *out);
 
