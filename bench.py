@@ -165,7 +165,7 @@ def run_reference(args, world, rank):
     name, n, d, k = datagen.CONFIGS[args.config]
     x = datagen.generate(args.config)
     eps = load_eps(args.config)
-    rows_per_step = args.ref_rows
+    rows_per_step = args.ref_step_rows
     cores = len(os.sched_getaffinity(0))
     os.environ.setdefault("OMP_NUM_THREADS", str(cores))
     rng = np.random.default_rng(12345)
@@ -229,7 +229,10 @@ def main():
     ap.add_argument("--refine", default="cuda", choices=["cuda", "tensor"],
                     help="refinement: CUDA cores (default) or the tensor-core prefilter with exact recheck")
     ap.add_argument("--batch-bytes", type=int, default=32 << 30)
-    ap.add_argument("--ref-rows", type=int, default=8000)
+    ap.add_argument("--ref-rows", type=int, default=8000,
+                    help="query rows of the cpu_baseline sample (about 18 s on 16 host cores)")
+    ap.add_argument("--ref-step-rows", type=int, default=2000,
+                    help="query rows per step of --impl reference (about 5 s per step on 16 host cores)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-batch-bytes", type=int, default=None,
