@@ -313,6 +313,14 @@ __device__ __forceinline__ bool exit_check_at(int k)
     return MQ == 8 || (k & 3) == 0;
 }
 
+// Box test: used up to d4 = 32, where the ring has 6 stages.  The producer
+// waits for its coordinate loads before it can store a tile's boxes; with
+// the 2-stage rings of larger d4 that wait starves the compute warps
+// (subspace, d = 64: 2.78 -> 3.13 s; spectrum, d = 128: 0.52 -> 0.57 s).
+#ifndef HISS_BOX_MAXD4
+#define HISS_BOX_MAXD4 32
+#endif
+
 // Resident blocks per SM the register budget is sized for.
 #ifndef HISS_REFINE_MINB
 #define HISS_REFINE_MINB 3
@@ -347,9 +355,14 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
     __shared__ int32_t s_nstart[kStencil];
     __shared__ int32_t s_vpre[kStencil + 1];
     __shared__ int64_t s_info[2];
+    // per stage and candidate half (32 rows, one compute warp's columns): the
+    // box of the staged candidates over the three index dimensions, lo at
+    // [0..2], hi at [4..6]
+    __shared__ __align__(16) float s_box[kMaxStages][kCandWarps][8];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d4 = D4 > 0 ? D4 : a.d4, S = tile_stride(d4), S2 = pair_stride(d4), C4 = d4 / 4;
+    const bool box = d4 <= HISS_BOX_MAXD4;  // box test over the three index dimensions
     const int nst = refine_stages<MQ, MP>(d4);
     float *Q2 = smem;
     float *P0 = smem + (kTQ / 2) * S2;
@@ -403,7 +416,9 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
         // ---- producer warp: stream the chunk through the stage ring ----
         // Each lane copies the 16-byte chunks of rows lane and lane + 32 of
         // a staged tile (cp.async), then arrives on the stage's full barrier
-        // twice: once asynchronously when its copies land, once now.
+        // twice: once asynchronously when its copies land, once now.  With
+        // the box test it first loads the rows' first 4 coordinates and
+        // stores the boxes of the tile's two halves.
         for (int it = 0; it < ntiles; ++it) {
             const int st = it % nst;
             const uint32_t round = (uint32_t)(it / nst);
@@ -413,11 +428,13 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
             }
             float *P = P0 + st * kTP * S;
             const int64_t v0 = vbeg + (int64_t)it * kTP;
+            float4 head[kTP / 32];  // first 4 coordinates of rows lane, lane + 32 (none: +inf)
 #pragma unroll
             for (int h = 0; h < kTP / 32; ++h) {
                 const int r = lane + 32 * h;
                 const int64_t v = v0 + r;
                 float4 *row = reinterpret_cast<float4 *>(P + r * S);
+                head[h] = make_float4(INFINITY, INFINITY, INFINITY, INFINITY);
                 if (v < vend) {
                     int lo = 0, hi = ncell - 1;  // last slot with s_vpre[slot] <= v
                     while (lo < hi) {
@@ -425,12 +442,38 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
                         if (s_vpre[mid] <= v) lo = mid; else hi = mid - 1;
                     }
                     const float *src = a.xs + (int64_t)(s_nstart[lo] + (int32_t)(v - s_vpre[lo])) * d4;
+                    if (box) head[h] = __ldg(reinterpret_cast<const float4 *>(src));
                     for (int cc = 0; cc < C4; ++cc) cp_async16(row + cc, src + 4 * cc);
                 } else {
                     // no candidate: -inf makes every distance to this row +inf
                     for (int cc = 0; cc < C4; ++cc)
                         row[cc] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
                 }
+            }
+            if (box) {
+                // box of each half over the three index dimensions (rows past
+                // the chunk end are left out; an empty half gets lo = +inf,
+                // hi = -inf)
+#pragma unroll
+                for (int h = 0; h < kTP / 32; ++h) {
+                    const bool has = head[h].x != INFINITY;
+                    float l0 = head[h].x, l1 = head[h].y, l2 = head[h].z;
+                    float h0 = has ? l0 : -INFINITY, h1 = has ? l1 : -INFINITY, h2 = has ? l2 : -INFINITY;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        l0 = fminf(l0, __shfl_xor_sync(0xffffffffu, l0, o));
+                        l1 = fminf(l1, __shfl_xor_sync(0xffffffffu, l1, o));
+                        l2 = fminf(l2, __shfl_xor_sync(0xffffffffu, l2, o));
+                        h0 = fmaxf(h0, __shfl_xor_sync(0xffffffffu, h0, o));
+                        h1 = fmaxf(h1, __shfl_xor_sync(0xffffffffu, h1, o));
+                        h2 = fmaxf(h2, __shfl_xor_sync(0xffffffffu, h2, o));
+                    }
+                    if (lane == 0) {
+                        *reinterpret_cast<float4 *>(&s_box[st][h][0]) = make_float4(l0, l1, l2, 0.f);
+                        *reinterpret_cast<float4 *>(&s_box[st][h][4]) = make_float4(h0, h1, h2, 0.f);
+                    }
+                }
+                __syncwarp();
             }
             cp_async_arrive_on(&s_full[st]);
             mbar_arrive(&s_full[st]);
@@ -462,6 +505,29 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
     uint32_t my_count = 0;                   // neighbours of query row qbase + 4 lp (lp < MQ)
     const int64_t row_word0 = a.tile_word[t] - a.word0;
     uint64_t prof_alg = 0, prof_exec = 0;
+    // box of the warp's query rows (wq * 4 MQ ... + 4 MQ - 1) over the three
+    // index dimensions; no query row: lo = +inf, hi = -inf
+    float qlo0, qlo1, qlo2, qhi0, qhi1, qhi2;
+    {
+        const int r = wq * (4 * MQ) + (lane & (4 * MQ - 1));
+        qlo0 = qlo1 = qlo2 = INFINITY;
+        qhi0 = qhi1 = qhi2 = -INFINITY;
+        if (r < nq) {
+            const float4 f = *reinterpret_cast<const float4 *>(a.xq + (int64_t)(q0 + r) * d4);
+            qlo0 = qhi0 = f.x;
+            qlo1 = qhi1 = f.y;
+            qlo2 = qhi2 = f.z;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            qlo0 = fminf(qlo0, __shfl_xor_sync(0xffffffffu, qlo0, o));
+            qlo1 = fminf(qlo1, __shfl_xor_sync(0xffffffffu, qlo1, o));
+            qlo2 = fminf(qlo2, __shfl_xor_sync(0xffffffffu, qlo2, o));
+            qhi0 = fmaxf(qhi0, __shfl_xor_sync(0xffffffffu, qhi0, o));
+            qhi1 = fmaxf(qhi1, __shfl_xor_sync(0xffffffffu, qhi1, o));
+            qhi2 = fmaxf(qhi2, __shfl_xor_sync(0xffffffffu, qhi2, o));
+        }
+    }
 
     for (int it = 0; it < ntiles; ++it) {
         const int st = it % nst;
@@ -472,12 +538,27 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
         }
         const int64_t v0 = vbeg + (int64_t)it * kTP;
         const float *P = P0 + st * kTP * S;
+        // Box test over the three index dimensions: for every pair of the
+        // warp tile, |q_k - p_k| rounded is at least the rounded box gap g_k,
+        // and the kernel's first three operations are e0 * e0, then fused
+        // e1 * e1 + s, e2 * e2 + s, so with rounding monotone G below is at
+        // most each pair's float32 partial sum after 3 dimensions, which the
+        // later terms only increase.  G > eps^2: every pair's bit is 0.
+        bool far = false;
+        if (box) {
+            const float4 plo = *reinterpret_cast<const float4 *>(&s_box[st][wp][0]);
+            const float4 phi = *reinterpret_cast<const float4 *>(&s_box[st][wp][4]);
+            const float g0 = fmaxf(0.f, fmaxf(__fsub_rn(plo.x, qhi0), __fsub_rn(qlo0, phi.x)));
+            const float g1 = fmaxf(0.f, fmaxf(__fsub_rn(plo.y, qhi1), __fsub_rn(qlo1, phi.y)));
+            const float g2 = fmaxf(0.f, fmaxf(__fsub_rn(plo.z, qhi2), __fsub_rn(qlo2, phi.z)));
+            far = __fmaf_rn(g2, g2, __fmaf_rn(g1, g1, __fmul_rn(g0, g0))) > eps2;
+        }
         f32x2 acc[MQ / 2][MP];
         if constexpr (PROF) {
             // all dimensions, counting live pairs step by step: the
             // method's per-pair exit every 4 dimensions (prof_alg) and the
             // warp schedule of the kernel below (prof_exec)
-            bool warp_live = true, surv = false;
+            bool warp_live = !far, surv = false;
             block_step2<MQ, MP, true>(acc, Q2, P, S2, S, pidbase, pbase, 0);
             int valid = 0;
 #pragma unroll
@@ -485,7 +566,7 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
 #pragma unroll
                 for (int j = 0; j < MP; ++j) valid += (qbase + 4 * i < nq && v0 + pbase + 8 * j < vend) ? 1 : 0;
             prof_alg += (uint64_t)valid * (uint64_t)min(4, a.d);
-            prof_exec += (uint64_t)valid * (uint64_t)min(2, a.d);
+            if (warp_live) prof_exec += (uint64_t)valid * (uint64_t)min(2, a.d);
             int live = 0;
             for (int k = 2; k < d4; k += 2) {
                 if (warp_live && !surv && exit_check_at<MQ>(k) &&
@@ -507,7 +588,7 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
                 else if (warp_live) prof_exec += (uint64_t)valid * (uint64_t)max(0, min(2, a.d - k));
                 block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k);
             }
-        } else {
+        } else if (!far) {
             block_step2<MQ, MP, true>(acc, Q2, P, S2, S, pidbase, pbase, 0);
             // warp-level early termination (the pairs are in variance order,
             // most leave early)

@@ -274,8 +274,10 @@ int hiss_set_option(hiss_ctx *ctx, int option, int64_t value);
  * the first multiple of 4 dimensions whose variance-ordered float32 partial
  * sum exceeds eps^2 (capped at d) -- the method's minimal refinement work
  * with early termination (RT-HiSS Section IV-A); out[1] = the dimensions
- * hiss_join's refinement kernel actually evaluates, whose warps abandon a
- * block of pairs only when all of them exceed eps^2 (checked after every 2
+ * hiss_join's refinement kernel actually evaluates, whose warps skip a
+ * block of pairs when the boxes of its queries and candidates over the three
+ * index dimensions are farther apart than eps, and otherwise abandon it only
+ * when all of its pairs exceed eps^2 (checked after every 2
  * dimensions up to d4 = 64, every 4 above); from d4 = 64 on, a warp left
  * with at most 64 pairs within eps^2 after 16 (d4 = 64) or 48 (d4 > 64)
  * dimensions finishes those pairs alone, each stopping when it exceeds
