@@ -87,6 +87,20 @@ def generate(cfg: int, n: int | None = None) -> np.ndarray:
     return np.ascontiguousarray(x.astype(np.float32))
 
 
+def lattice(n: int, d: int, seed: int, side: int = 20, p_low: float = 0.1) -> np.ndarray:
+    """Integer points for exact-boundary tests: the first min(d, 3)
+    coordinates uniform on {0, ..., side - 1}, the others 1 with probability
+    p_low and 0 otherwise (so the first three have the largest variance).
+    Every squared distance is a small integer, exact in float32."""
+    rng = np.random.default_rng([MASTER_SEED, 99, int(n), int(d), int(seed)])
+    x = np.zeros((n, d), dtype=np.float64)
+    k = min(d, 3)
+    x[:, :k] = rng.integers(0, side, size=(n, k))
+    if d > k:
+        x[:, k:] = (rng.random((n, d - k)) < p_low).astype(np.float64)
+    return np.ascontiguousarray(x.astype(np.float32))
+
+
 def sample_queries(n: int, m: int, seed: int) -> np.ndarray:
     """m distinct query indices in [0, n), drawn without replacement."""
     return np.random.default_rng(seed).choice(n, size=min(m, n), replace=False).astype(np.int64)

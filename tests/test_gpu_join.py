@@ -90,6 +90,26 @@ def test_eps_zero_duplicates_and_single_point():
     assert rows[0].tolist() == [0] and counts.tolist() == [1]
 
 
+@pytest.mark.parametrize("d", [3, 16, 32, 64, 128])
+@pytest.mark.parametrize("eps", [2.0, 3.0])
+def test_exact_boundary_on_integer_lattice(d, eps):
+    """Integer coordinates make every float32 operation of the refinement
+    exact, so the rows must equal the definition with no tolerance band:
+    pairs at exactly eps are in, pairs beyond are out.  Many pairs lie
+    exactly on the boundary, among them pairs whose query and candidate
+    boxes over the three index dimensions are exactly eps apart, which the
+    warp-tile box test must not skip (d <= 32), and pairs that the survivor
+    mode finishes one per lane (d = 64, 128)."""
+    x = datagen.lattice(4000, d, seed=d, p_low=min(0.1, 1.2 / max(d - 3, 1)))
+    rows, counts, _ = _join(x, eps)
+    row_ptr, cols, _, dist2 = oracle.rows(x, eps, np.arange(len(x)), band=0.0)
+    assert np.any(dist2 == eps * eps), "no pair exactly on the boundary"
+    for q in range(len(x)):
+        want = cols[row_ptr[q]:row_ptr[q + 1]]
+        assert np.array_equal(np.sort(rows[q]), want), "row %d differs" % q
+        assert counts[q] >= want.size
+
+
 def test_eps_covering_everything_and_tiny_eps():
     x = datagen.generate(1, n=1200)
     rows, counts, _ = _join(x, 10.0)
