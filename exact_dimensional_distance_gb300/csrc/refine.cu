@@ -304,13 +304,21 @@ __device__ __forceinline__ void survivors(const f32x2 (&acc)[MQ / 2][MP], const 
 }
 
 // Where a warp checks for early termination (k = dimensions summed so far):
-// with 8 x 4 blocks (d4 <= 64) after every 2 dimensions, with 4 x 4 blocks
-// after every 4 (there the pairs leave later, and the shorter steps need two
-// per loop iteration to overlap their loads).
-template <int MQ>
-__device__ __forceinline__ bool exit_check_at(int k)
+// with 8 x 4 blocks (d4 <= 64) after every 2 dimensions from the first check
+// on, with 4 x 4 blocks after every 4 (there the pairs leave later, and the
+// shorter steps need two per loop iteration to overlap their loads).  Where
+// the box test runs, it has already removed most of the tiles that an early
+// check would end, so the first check comes later: after 6 dimensions at
+// d4 = 32 and 10 at d4 = 16 (gmm refinement 35.2 ms with the first check
+// after 2, 34.4 after 6; exp 15.3 s after 2, 14.7 s after 10).
+__host__ __device__ __forceinline__ constexpr int first_check(int d4)
 {
-    return MQ == 8 || (k & 3) == 0;
+    return d4 == 16 ? 10 : (d4 == 32 ? 6 : 2);
+}
+template <int MQ>
+__device__ __forceinline__ bool exit_check_at(int k, int d4)
+{
+    return MQ == 8 ? k >= first_check(d4) : (k & 3) == 0;
 }
 
 // Box test: used up to d4 = 32, where the ring has 6 stages.  The producer
@@ -569,7 +577,7 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
             if (warp_live) prof_exec += (uint64_t)valid * (uint64_t)min(2, a.d);
             int live = 0;
             for (int k = 2; k < d4; k += 2) {
-                if (warp_live && !surv && exit_check_at<MQ>(k) &&
+                if (warp_live && !surv && exit_check_at<MQ>(k, d4) &&
                     __all_sync(0xffffffffu, block_min<MQ, MP>(acc) > eps2))
                     warp_live = false;
                 if ((k & 3) == 0) {
@@ -600,7 +608,7 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
                         any_close = __any_sync(0xffffffffu, block_min<MQ, MP>(acc) <= eps2);
                         break;
                     }
-                    if (exit_check_at<MQ>(k) && __all_sync(0xffffffffu, block_min<MQ, MP>(acc) > eps2)) {
+                    if (exit_check_at<MQ>(k, d4) && __all_sync(0xffffffffu, block_min<MQ, MP>(acc) > eps2)) {
                         any_close = false;
                         break;
                     }
