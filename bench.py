@@ -72,6 +72,32 @@ def peaks():
         return {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0}, "fallback"
 
 
+def join_algorithmic_bytes(j, st, n, d):
+    """Algorithmic bytes of one whole join (build, index, count, refinement,
+    compaction), from the index's cell sizes and stencils:
+      index   4 N d (statistics) + 24 N per sort digit pass (key and value
+              read and written) + 8 N d4 (variance-ordered copy and gather)
+              + 16 C + 4 P (cell ranges and stencil lists);
+      points  4 N d4 (query rows) + sum over cells i of the candidate rows
+              of i's stencil, 4 d4 bytes each, once per query tile of i;
+      results K_c / 8 written and read (one mask bit per candidate pair)
+              + 4 |R| + 8 N (CSR columns and row offsets)."""
+    import numpy as np
+    ix = j.index()
+    cs = ix["cell_start"].cpu().numpy().astype(np.int64)
+    size = np.diff(cs)
+    bound = ix["cell_bound"].cpu().numpy().astype(np.int64)
+    d4 = int(st["d_pad"])
+    tq = 128 if d4 <= 64 else 64
+    tiles = (size + tq - 1) // tq
+    passes = (int(st["key_bits"]) + 7) // 8
+    C, P, K, R = st["cells"], st["cell_pairs"], st["candidates"], st["pairs"]
+    index = 4 * n * d + 24 * n * passes + 8 * n * d4 + 16 * C + 4 * P
+    points = 4 * n * d4 + 4 * d4 * int((tiles * bound).sum())
+    results = K / 8 + K / 8 + 4 * R + 8 * n
+    return {"index": float(index), "points": float(points), "results": float(results)}
+
+
 def fp32_peak_tflops(sm_mhz):
     """FP32 pipe peak for the refinement's instruction mix: 152 SMs x 128 FP32
     lanes x clock; one pair-dimension is a subtract (1 flop) and a fused
@@ -325,7 +351,8 @@ def main():
     pk, pk_kind = peaks()
     peak = fp32_peak_tflops(pk.get("sm_max_mhz", 2070.0))
     achieved = flops / (refine_ms / 1e3) / 1e12
-    tpu = refine_traffic_per_unit()
+    # DRAM traffic per unit was captured on the full gmm workload only
+    tpu = refine_traffic_per_unit() if args.config == 2 and args.n is None else None
     roofline = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": None if tpu is None else tpu * st["refine_units"] / refine_launches,
                 "traffic_unit": "bytes per launch (ncu DRAM read+write, scaled by units)", "kernel": "k_refine",
@@ -337,6 +364,21 @@ def main():
                 "full_dims_frac": 3.0 * cand * d / (refine_ms / 1e3) / 1e12 / peak,
                 "peak_kind": "FP32 lanes x %s sm_max_mhz x 1.5 flop" % pk_kind}
 
+    # whole-join roofline: the slower of the refinement's algorithmic flops at
+    # the FP32 peak and the join's algorithmic bytes at the HBM peak, against
+    # the measured step time
+    jb = join_algorithmic_bytes(j, st, n, d)
+    jbytes = sum(jb.values())
+    hbm = float(pk.get("hbm_gbs", 6800.0))
+    t_flop = flops / (peak * 1e12) * 1e3
+    t_bytes = jbytes / (hbm * 1e9) * 1e3
+    t_join = 1e3 * t_local / args.steps
+    join_roofline = {"bound": "fp32" if t_flop >= t_bytes else "hbm", "flop": flops, "bytes": jbytes,
+                     "bytes_split": jb, "t_flop_ms": t_flop, "t_bytes_ms": t_bytes,
+                     "t_roof_ms": max(t_flop, t_bytes), "t_join_ms": t_join,
+                     "frac": max(t_flop, t_bytes) / t_join, "fp32_peak_tflops": peak, "hbm_gbs": hbm,
+                     "peak_kind": pk_kind}
+
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True,
             "scaling": "strong" if args.shard else "weak", "vs_baseline": None, "dtype": "f32",
@@ -347,7 +389,8 @@ def main():
             "pruning": 1.0 - cand / float(n) ** 2,
             "phase_ms": {k: st[k] for k in ("ms_build", "ms_index", "ms_count", "ms_refine", "ms_compact",
                                             "ms_deliver")},
-            "batches": st["batches"], "cells": st["cells"], "clocks": clocks, "roofline": roofline}
+            "batches": st["batches"], "cells": st["cells"], "clocks": clocks, "roofline": roofline,
+            "join_roofline": join_roofline}
 
     if not args.no_e2e:
         # end to end through the host-buffer entry points
