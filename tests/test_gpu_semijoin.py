@@ -52,6 +52,22 @@ def test_semi_join_matches_oracle(cfg, nd, nq, eps):
     assert np.all(counts >= true)
 
 
+def test_semi_count_bound_hand_case_on_gpu():
+    # the hand-computed bounds of tests/golden/semi_bound_hand.txt: queries one
+    # and two cells outside D's grid, below and above, on every index dimension
+    from test_oracle import semi_bound_hand_case
+    edd = _edd()
+    xq, xd, eps, want = semi_bound_hand_case()
+    j = edd.Join()
+    j.build(torch.from_numpy(xd).cuda())
+    qd = torch.from_numpy(xq).cuda()
+    counts = j.count_queries(qd, eps).cpu().numpy()
+    rows = j.join_queries_sets(qd, eps)
+    j.close()
+    assert counts.tolist() == want
+    _check(xq, xd, eps, rows)
+
+
 def test_semi_join_with_queries_equal_to_data_is_self_join_and_self_join_still_works():
     edd = _edd()
     x = datagen.generate(1, n=2500)

@@ -1,5 +1,7 @@
 """Pins for the CPU oracle: hand-computed cases, the pages' worked examples,
 invariants of the definition and brute force on tiny inputs.  CPU only."""
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -111,13 +113,48 @@ def test_pick_eps_sample_identity():
     assert int(np.sum(pooled <= e2)) == len(q) * k            # mean K, self excluded
 
 
+def _retry_instance():
+    """One dense query among sparse ones: its first M = 64 kept distances all
+    lie below the pooled (nq K + 1)-th value, so the picker must retry with a
+    larger M before its answer is exact (RT-HiSS Section V-B defines the
+    selectivity the picker targets)."""
+    rng = np.random.default_rng(21)
+    dense = (rng.random((100, 3)) * 1e-3).astype(np.float32)            # 100 points within 1e-3
+    sparse = (rng.random((500, 3)) * 40.0 + 2.0).astype(np.float32)     # far from the dense ball
+    x = np.concatenate([dense, sparse])
+    q = np.r_[0, 100 + np.arange(9) * 50].astype(np.int64)              # 1 dense query, 9 sparse
+    return x, q, 10
+
+
+def _pooled(x, q):
+    x64 = x.astype(np.float64)
+    return np.sort(np.concatenate([np.delete(((x64 - x64[i]) ** 2).sum(1), i) for i in q]))
+
+
 def test_pick_eps_retry_path():
-    # many equal distances force the kept-prefix check to ask for a larger M
+    x, q, k = _retry_instance()
+    # the first attempt keeps M = max(4 K, 64) distances per query and must ask for more
+    a, b = ctypes.c_double(), ctypes.c_double()
+    rc = oracle._lib().orc_pick_eps2(x.ctypes.data, len(x), x.shape[1], q.ctypes.data, q.size, k, 64,
+                                     ctypes.byref(a), ctypes.byref(b))
+    assert rc == 1
+    pooled = _pooled(x, q)
+    assert a.value != pooled[q.size * k - 1]          # the truncated pool alone would be wrong
+    r = oracle.pick_eps(x, k, q)
+    assert r["a"] == pooled[q.size * k - 1]
+    assert r["b"] == pooled[q.size * k]
+    e2 = oracle.eps_squared(r["eps"])
+    assert int(np.sum(pooled <= e2)) == q.size * k
+
+
+def test_pick_eps_many_equal_distances():
+    # 20 groups of 20 equal points: a = b; the picker still returns a <= eps^2
     x = np.zeros((400, 2), dtype=np.float32)
     x[:, 0] = np.repeat(np.arange(20), 20).astype(np.float32)
     q = np.arange(0, 400, 40)
     r = oracle.pick_eps(x, 30, q)
-    assert r["a"] <= r["b"]
+    pooled = _pooled(x, q)
+    assert r["a"] == pooled[q.size * 30 - 1] and r["b"] == pooled[q.size * 30]
 
 
 # ---------------- index pins -----------------------------------------------
@@ -227,6 +264,24 @@ def test_semi_join_hand_case():
     rows = [sorted(cols[row_ptr[i]:row_ptr[i + 1]].tolist()) for i in range(4)]
     assert rows == [[0, 1], [1], [2], []]          # |(6,8)-(3,4)| = 5 inclusive; (13,4)-(10,0) = 5
     assert oracle.semi_brute_force_py(xq, xd, 5.0) == [{0, 1}, {1}, {2}, set()]
+
+
+def semi_bound_hand_case():
+    """The hand-computed semi-join count bounds of tests/golden/semi_bound_hand.txt."""
+    g = read_golden("semi_bound_hand.txt")
+    xd = np.array([[float(v) for v in vals] for t, vals in g if t == "d"], np.float32)
+    xq = np.array([[float(v) for v in vals[:3]] for t, vals in g if t == "q"], np.float32)
+    want = [int(vals[3]) for t, vals in g if t == "q"]
+    eps = float([vals for t, vals in g if t == "eps"][0][0])
+    return xq, xd, eps, want
+
+
+def test_semi_count_bound_hand_case():
+    # queries inside, one and two cells outside D's grid on each index
+    # dimension, below and above, on a variance order that is not the identity
+    xq, xd, eps, want = semi_bound_hand_case()
+    assert oracle.grid(xd, eps)["perm"].tolist() == [1, 2, 0]
+    assert oracle.semi_count_bound(xq, xd, eps).tolist() == want
 
 
 def test_semi_join_with_q_equal_d_is_self_join():

@@ -28,6 +28,7 @@ MUTANTS = {
     "picker_keeps_self": ("if (j != i) buf[m++]", "buf[m++]"),
     "picker_off_by_one": ("const double a = pool[nq * K - 1], b = pool[nq * K];",
                           "const double a = pool[nq * K], b = pool[nq * K + 1];"),
+    "picker_never_retries": ("if (!(b < kth[r])) { status = 1; break; }", "if (0) { status = 1; break; }"),
 }
 
 
@@ -78,7 +79,23 @@ def _pins_hold(lib) -> bool:
                            ctypes.byref(a), ctypes.byref(b))
     x64 = x.astype(np.float64)
     pooled = np.sort(np.concatenate([np.delete(((x64 - x64[i]) ** 2).sum(1), i) for i in q]))
-    return rc == 0 and a.value == pooled[q.size * 5 - 1] and b.value == pooled[q.size * 5]
+    if not (rc == 0 and a.value == pooled[q.size * 5 - 1] and b.value == pooled[q.size * 5]):
+        return False
+    # the retry path: one dense query among sparse ones, M grown as oracle.pick_eps grows it
+    rng = np.random.default_rng(21)
+    x = np.concatenate([(rng.random((100, 3)) * 1e-3).astype(np.float32),
+                        (rng.random((500, 3)) * 40.0 + 2.0).astype(np.float32)])
+    q = np.r_[0, 100 + np.arange(9) * 50].astype(np.int64)
+    m = 64
+    while True:
+        rc = lib.orc_pick_eps2(x.ctypes.data, len(x), x.shape[1], q.ctypes.data, q.size, 10, m,
+                               ctypes.byref(a), ctypes.byref(b))
+        if rc != 1 or m > 4 * len(x):
+            break
+        m *= 4
+    x64 = x.astype(np.float64)
+    pooled = np.sort(np.concatenate([np.delete(((x64 - x64[i]) ** 2).sum(1), i) for i in q]))
+    return rc == 0 and a.value == pooled[q.size * 10 - 1] and b.value == pooled[q.size * 10]
 
 
 def test_real_oracle_passes_mutant_pins(tmp_path):
@@ -146,3 +163,41 @@ def test_knn_pins_hold_for_the_oracle():
 def test_knn_pins_catch_planted_mistakes(kind):
     with pytest.raises(AssertionError):
         _knn_pins(_knn_variant(kind))
+
+
+# ---- semi-join count bound: planted mistakes in copies of its Python source ---
+
+SEMI_BOUND_MUTANTS = {
+    "stencil_radius_2": ("for dx, dy, dz in STENCIL:",
+                         "for dx, dy, dz in [(a, b, c) for c in range(-2, 3) for b in range(-2, 3) "
+                         "for a in range(-2, 3)]:"),
+    "unsigned_clip": ("cq[:, k] = np.floor(u).astype(np.int64)",
+                      "cq[:, k] = np.maximum(np.floor(u), 0).astype(np.int64)"),
+    "truncate_not_floor": ("cq[:, k] = np.floor(u).astype(np.int64)", "cq[:, k] = u.astype(np.int64)"),
+    "original_dimension_order": ('idx = g["perm"][: min(3, xd.shape[1])]', "idx = np.arange(min(3, xd.shape[1]))"),
+    "origin_from_queries": ('- g["origin"][k]) / w', '- xq[:, idx[k]].min()) / w'),
+}
+
+
+def _semi_bound_variant(name):
+    import inspect
+    import textwrap
+    src = textwrap.dedent(inspect.getsource(oracle.semi_count_bound))
+    old, new = SEMI_BOUND_MUTANTS[name]
+    assert old in src, name
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new), "<mutant %s>" % name, "exec"), ns)
+    return ns["semi_count_bound"]
+
+
+def test_semi_bound_pin_holds_for_the_oracle():
+    from test_oracle import semi_bound_hand_case
+    xq, xd, eps, want = semi_bound_hand_case()
+    assert oracle.semi_count_bound(xq, xd, eps).tolist() == want
+
+
+@pytest.mark.parametrize("name", sorted(SEMI_BOUND_MUTANTS))
+def test_semi_bound_mutant_is_caught(name):
+    from test_oracle import semi_bound_hand_case
+    xq, xd, eps, want = semi_bound_hand_case()
+    assert _semi_bound_variant(name)(xq, xd, eps).tolist() != want, "pin did not catch %s" % name
