@@ -31,7 +31,9 @@ int64_t *g_scratch_addr[kMaxDevices] = {};
 
 // Device address of g_scan_scratch on the current device.  In host code the
 // symbol name is only a host-side stand-in, so the address is looked up once
-// per device (with that device current) and cached.
+// per device (with that device current) and cached.  cudaDeviceReset destroys
+// the module that holds the array; the cached address is then stale, so a
+// process that resets a device must not call this entry point on it again.
 cudaError_t scratch_address(int64_t **out)
 {
     int dev = 0;
@@ -53,7 +55,10 @@ extern "C" int hiss_exclusive_scan_noalloc(void *cuda_stream, const int64_t *d_i
 {
     if (n < 0 || n > kNoallocMaxN || !d_out || (n > 0 && !d_in)) return HISS_E_ARG;
     if (hiss::scan_tmp_elems(n + 1) > kNoallocScratchElems) return HISS_E_ARG;
-    cudaGetLastError();  // drop a stale non-sticky error left by an earlier runtime call
+    // A pending error from the caller's own earlier work is left in place for
+    // the caller to read (cudaGetLastError would clear it); this call does not
+    // run on top of it, since its own launch check could not tell the two apart.
+    if (cudaPeekAtLastError() != cudaSuccess) return HISS_E_CUDA;
     int64_t *scratch = nullptr;
     if (scratch_address(&scratch) != cudaSuccess) return HISS_E_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);

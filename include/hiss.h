@@ -332,10 +332,17 @@ int hiss_gram_tf32(hiss_ctx *ctx, const float *d_a, const float *d_b, int32_t k,
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any
  *     stream capture.
+ *   - cudaDeviceReset makes the cached address stale: after resetting a
+ *     device, do not call this entry point on it again in the same process.
  *   - All calls share the array: calls whose kernels may overlap on the GPU
  *     (other streams, other host threads) race and must be ordered by the
  *     caller.  Nothing in the array needs clearing between calls.
- * Returns HISS_OK, HISS_E_ARG, or HISS_E_CUDA if a launch failed. */
+ *   - A CUDA error already pending on the calling thread (left by the
+ *     caller's earlier work) is not cleared: the call returns HISS_E_CUDA
+ *     without launching, and the caller can still read the error with
+ *     cudaGetLastError.
+ * Returns HISS_OK, HISS_E_ARG, or HISS_E_CUDA if a launch failed or an error
+ * was already pending. */
 int hiss_exclusive_scan_noalloc(void *cuda_stream, const int64_t *d_in, int64_t *d_out, int64_t n);
 
 #ifdef __cplusplus
