@@ -72,6 +72,7 @@ struct hiss_ctx {
     // overlapped host delivery (CSR to host): second set of batch outputs and
     // pinned staging, a copy stream and its events (created on first use)
     DBuf row_ptr2, cols2, query_ids2, query_rows2;
+    DBuf row_ptr_sub;  // row offsets of a batch delivered in parts
     void *h_pinned2 = nullptr;
     size_t h_cap2 = 0;
     cudaStream_t copy_stream = nullptr;
@@ -535,7 +536,15 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
         CK(cudaMemGetInfo(&fr, &tot));
         batch_bytes = fr / 4;
     }
-    const int64_t cap_words = (int64_t)(batch_bytes / 4);
+    // batch_bytes bounds a batch's device memory.  The planner fits the mask,
+    // its occupancy bitmap and the per-query arrays (counts, row offsets, ids;
+    // doubled for the overlapped host delivery) in three quarters of it; the
+    // CSR columns get the rest.  A batch whose result outgrows that is
+    // compacted and delivered in several parts (RT-HiSS Section IV-D sizes
+    // batches so that their results fit in device memory).
+    const int64_t per_query_words = (24 + (mode == HISS_OUT_MASK ? 16 : 0) + (ov ? 20 : 0)) / 4;
+    const int64_t budget_words = (int64_t)(batch_bytes / 4);
+    const int64_t cap_words = budget_words - budget_words / 4;
     if (thi < 0) thi = ctx->T;
     const int64_t T = thi - tlo;  // tiles of this call; batch tile indices are relative to tlo
     ST(ensure(ctx, ctx->boundaries, 8 * (size_t)(T + 2)));
@@ -543,7 +552,7 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
     ST(ensure(ctx, ctx->nb_d, 64));
     CK(cudaMemsetAsync(ctx->flags.p, 0, sizeof(int) * kNumFlags, s));
     CK(plan_batches(as<int64_t>(ctx->tile_word) + tlo, as<int64_t>(ctx->tile_unit) + tlo,
-                    as<int64_t>(ctx->tile_qoff) + tlo, T, cap_words, as<int64_t>(ctx->boundaries),
+                    as<int64_t>(ctx->tile_qoff) + tlo, T, cap_words, per_query_words, as<int64_t>(ctx->boundaries),
                     as<int64_t>(ctx->binfo), as<int64_t>(ctx->nb_d), as<int>(ctx->flags), s, &ctx->launches));
     int64_t nb = 0;
     int hflags[kNumFlags];
@@ -555,11 +564,15 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
     CK(cudaMemcpyAsync(info.data(), ctx->binfo.p, 32 * (size_t)(nb + 1), cudaMemcpyDeviceToHost, s));
     ST(sync(ctx));
 
-    int64_t max_words = 0, max_nq = 0;
+    int64_t max_words = 0, max_nq = 0, max_cost = 0;
     for (int64_t b = 0; b < nb; ++b) {
-        max_words = std::max(max_words, info[4 * (b + 1)] - info[4 * b]);
-        max_nq = std::max(max_nq, info[4 * (b + 1) + 2] - info[4 * b + 2]);
+        const int64_t dw = info[4 * (b + 1)] - info[4 * b], dq = info[4 * (b + 1) + 2] - info[4 * b + 2];
+        max_words = std::max(max_words, dw);
+        max_nq = std::max(max_nq, dq);
+        max_cost = std::max(max_cost, dw + (dw >> 5) + 2 + per_query_words * dq);
     }
+    // CSR columns per delivery (per slot with the overlapped delivery)
+    const int64_t cols_cap = std::max<int64_t>(1, (budget_words - max_cost) / (ov ? 2 : 1));
     ST(ensure(ctx, ctx->mask, 4 * (size_t)max_words));
     ST(ensure(ctx, ctx->occ, 4 * (size_t)(max_words / 32 + 2)));
     ST(ensure(ctx, ctx->qcount, 4 * (size_t)(max_nq + 1)));
@@ -582,7 +595,18 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
     hiss_batch pending_hb{};
 
     double ms_refine = 0.0, ms_compact = 0.0, ms_deliver = 0.0;
-    int64_t pairs = 0;
+    int64_t pairs = 0, delivered = 0;
+    // Hands over the overlapped delivery still in flight, if any.
+    auto flush_pending = [&]() -> int {
+        if (pending < 0) return HISS_OK;
+        CK(cudaEventSynchronize(ctx->ev_copied[pslot]));
+        float cms = 0.0f;
+        if (cudaEventElapsedTime(&cms, ctx->ev_copy0[pslot], ctx->ev_copied[pslot]) == cudaSuccess) ms_deliver += cms;
+        cudaGetLastError();
+        pending = -1;
+        if (fn && fn(user, &pending_hb) != 0) return HISS_E_CALLBACK;
+        return HISS_OK;
+    };
     for (int64_t b = 0; b < nb; ++b) {
         const int64_t *lo = &info[4 * b], *hi = &info[4 * (b + 1)];
         const int64_t nq = hi[2] - lo[2];
@@ -654,6 +678,69 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
                            &ctx->launches));
         CK(cudaMemcpyAsync(&nnz, as<int64_t>(rp_buf) + nq, 8, cudaMemcpyDeviceToHost, s));
         ST(sync(ctx));
+        if (mode == HISS_OUT_CSR && nnz > cols_cap) {
+            // The batch's result does not fit its CSR budget: compact and
+            // deliver it in parts of consecutive queries, each within the
+            // budget, one after another on the context's stream.
+            ST(flush_pending());
+            std::vector<int64_t> rph((size_t)nq + 1);
+            CK(cudaMemcpyAsync(rph.data(), rp_buf.p, 8 * (size_t)(nq + 1), cudaMemcpyDeviceToHost, s));
+            ST(sync(ctx));
+            ms_refine += elapsed(ctx, 4, 5);
+            ST(ensure(ctx, ctx->cols, 4 * (size_t)cols_cap));
+            ST(ensure(ctx, ctx->row_ptr_sub, 8 * (size_t)(max_nq + 1)));
+            for (int64_t q = 0; q < nq;) {
+                int64_t e = q + 1;
+                if (rph[e] - rph[q] > cols_cap) return HISS_E_BATCH_TOO_SMALL;  // one row alone is larger
+                e = std::upper_bound(rph.begin() + e, rph.end(), rph[q] + cols_cap) - rph.begin() - 1;
+                const int64_t nsub = e - q, nnz_sub = rph[e] - rph[q];
+                CompactArgs cs = ca;
+                cs.q0 = ca.q0 + q;
+                cs.nq = nsub;
+                cs.row_ptr = as<int64_t>(rp_buf) + q;
+                cs.col0 = rph[q];
+                cs.row_ptr_out = as<int64_t>(ctx->row_ptr_sub);
+                cs.cols = as<int32_t>(ctx->cols);
+                cs.query_ids = as<int64_t>(ctx->query_ids);
+                cs.query_rows = as<int32_t>(ctx->query_rows);
+                CK(cudaEventRecord(ctx->ev[5], s));
+                CK(compact(cs, s, &ctx->launches));
+                CK(cudaEventRecord(ctx->ev[6], s));
+                hiss_batch hb{};
+                hb.index = delivered++;
+                hb.nq = nsub;
+                hb.nnz = nnz_sub;
+                hb.mode = mode;
+                if (to_host) {
+                    const size_t o_ids = 0, o_rp = align256(8 * nsub), o_rows = o_rp + align256(8 * (nsub + 1));
+                    const size_t o_data = o_rows + align256(4 * nsub);
+                    ST(ensure_pinned(ctx, o_data + 4 * (size_t)nnz_sub + 256));
+                    char *h = static_cast<char *>(ctx->h_pinned);
+                    CK(cudaMemcpyAsync(h + o_ids, ctx->query_ids.p, 8 * nsub, cudaMemcpyDeviceToHost, s));
+                    CK(cudaMemcpyAsync(h + o_rows, ctx->query_rows.p, 4 * nsub, cudaMemcpyDeviceToHost, s));
+                    CK(cudaMemcpyAsync(h + o_rp, ctx->row_ptr_sub.p, 8 * (nsub + 1), cudaMemcpyDeviceToHost, s));
+                    CK(cudaMemcpyAsync(h + o_data, ctx->cols.p, 4 * (size_t)nnz_sub, cudaMemcpyDeviceToHost, s));
+                    hb.query_ids = reinterpret_cast<const int64_t *>(h + o_ids);
+                    hb.row_ptr = reinterpret_cast<const int64_t *>(h + o_rp);
+                    hb.query_rows = reinterpret_cast<const int32_t *>(h + o_rows);
+                    hb.cols = reinterpret_cast<const int32_t *>(h + o_data);
+                    hb.on_host = 1;
+                } else {
+                    hb.query_ids = as<int64_t>(ctx->query_ids);
+                    hb.row_ptr = as<int64_t>(ctx->row_ptr_sub);
+                    hb.query_rows = as<int32_t>(ctx->query_rows);
+                    hb.cols = as<int32_t>(ctx->cols);
+                }
+                CK(cudaEventRecord(ctx->ev[7], s));
+                ST(sync(ctx));
+                ms_compact += elapsed(ctx, 5, 6);
+                ms_deliver += elapsed(ctx, 6, 7);
+                if (fn && fn(user, &hb) != 0) return HISS_E_CALLBACK;
+                q = e;
+            }
+            pairs += nnz;
+            continue;
+        }
         if (mode == HISS_OUT_CSR) {
             ST(ensure(ctx, cols_buf, 4 * (size_t)nnz));
             ca.row_ptr = as<int64_t>(rp_buf);
@@ -666,7 +753,7 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
         CK(cudaEventRecord(ctx->ev[6], s));
 
         hiss_batch hb{};
-        hb.index = b;
+        hb.index = delivered++;
         hb.nq = nq;
         hb.nnz = nnz;
         hb.mode = mode;
@@ -695,14 +782,10 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
             hb.on_host = 1;
             // hand over the previous batch, whose copies ran during this batch's refinement
             if (pending >= 0) {
-                CK(cudaEventSynchronize(ctx->ev_copied[pslot]));
-                float cms = 0.0f;
-                if (cudaEventElapsedTime(&cms, ctx->ev_copy0[pslot], ctx->ev_copied[pslot]) == cudaSuccess)
-                    ms_deliver += cms;
-                cudaGetLastError();
-                if (fn && fn(user, &pending_hb) != 0) {
+                const int r = flush_pending();
+                if (r != HISS_OK) {
                     cudaStreamSynchronize(cs);
-                    return HISS_E_CALLBACK;
+                    return r;
                 }
             }
             ST(sync(ctx));
@@ -757,16 +840,11 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
         pairs += nnz;
         if (fn && fn(user, &hb) != 0) return HISS_E_CALLBACK;
     }
-    if (pending >= 0) {
-        CK(cudaEventSynchronize(ctx->ev_copied[pslot]));
-        float cms = 0.0f;
-        if (cudaEventElapsedTime(&cms, ctx->ev_copy0[pslot], ctx->ev_copied[pslot]) == cudaSuccess) ms_deliver += cms;
-        cudaGetLastError();
-        if (fn && fn(user, &pending_hb) != 0) return HISS_E_CALLBACK;
-    }
+    ST(flush_pending());
     ST(check_flags(ctx));
     ctx->st.pairs = mode == HISS_OUT_CSR ? pairs : -1;
     ctx->st.batches = nb;
+    ctx->st.deliveries = delivered;
     ctx->st.query_tiles = T;
     ctx->st.refine_units = info[4 * (size_t)nb + 1] - info[1];
     ctx->st.mask_words_max = max_words;
@@ -1136,7 +1214,7 @@ void hiss_destroy(hiss_ctx *ctx)
                    &ctx->q_cell_of_row, &ctx->q_cell_start, &ctx->q_cell_key, &ctx->q_nbr, &ctx->q_nbr_cnt,
                    &ctx->q_bound, &ctx->q_work_key, &ctx->q_cell_idx, &ctx->q_work, &ctx->k_keys,
                    &ctx->k_vals, &ctx->k_keys_alt, &ctx->k_vals_alt, &ctx->k_sort_tmp, &ctx->k_d2, &ctx->k_prow,
-                   &ctx->k_done, &ctx->k_active, &ctx->row_ptr2, &ctx->cols2,
+                   &ctx->k_done, &ctx->k_active, &ctx->row_ptr2, &ctx->cols2, &ctx->row_ptr_sub,
                    &ctx->query_ids2, &ctx->query_rows2};
     if (ctx->copy_stream) cudaStreamSynchronize(ctx->copy_stream);
     for (DBuf *b : all) release(ctx, *b);

@@ -86,10 +86,12 @@ cudaError_t tile_fill(const uint32_t *order, const int32_t *cell_start, const in
 // Greedy batches over query tiles: boundaries[k] = first tile of batch k,
 // boundaries[nb] = T; *nb written to nb_out (device).  info[4 k + 0..2] =
 // (word offset, unit offset, query offset) at boundary k, for k = 0..nb.
-// flags[kFlagPlanTooSmall] is set when one tile's mask exceeds cap_words.
+// A batch's cost in 32-bit words is its mask words + occupancy words
+// (words / 32 + 2) + per_query_words per query; it is at most cap_words.
+// flags[kFlagPlanTooSmall] is set when one tile alone exceeds cap_words.
 cudaError_t plan_batches(const int64_t *tile_word_off, const int64_t *tile_unit, const int64_t *tile_qoff,
-                         int64_t T, int64_t cap_words, int64_t *boundaries, int64_t *info, int64_t *nb_out,
-                         int *flags, cudaStream_t s, int64_t *launches);
+                         int64_t T, int64_t cap_words, int64_t per_query_words, int64_t *boundaries, int64_t *info,
+                         int64_t *nb_out, int *flags, cudaStream_t s, int64_t *launches);
 
 // ---- refinement and compaction (refine.cu) ---------------------------------
 struct RefineArgs {
@@ -137,6 +139,8 @@ struct CompactArgs {
     const uint32_t *mask;
     const uint32_t *occ;        // occupancy bitmap of the mask (nonzero words)
     const int64_t *row_ptr;     // [nq+1] batch-relative
+    int64_t col0;               // row_ptr value of this call's first query: row gq goes to cols + row_ptr[gq] - col0
+    int64_t *row_ptr_out;       // [nq+1] row_ptr - col0 (may be NULL)
     int32_t *cols;              // CSR output (NULL: only query ids/rows/cand)
     int64_t *query_ids;         // [nq]
     int32_t *query_rows;        // [nq]

@@ -345,10 +345,20 @@ __global__ void k_tile_fill(const uint32_t *__restrict__ order, const int32_t *_
     }
 }
 
-// Greedy batches: each batch takes the longest run of tiles whose masks fit
-// in cap_words.  One thread; the number of batches is small.
+// Greedy batches: each batch takes the longest run of tiles whose device
+// memory fits in cap_words 32-bit words: the mask words, their occupancy
+// bitmap (one bit per word, plus two words of slack) and per_query words for
+// each query (counts, row offsets, ids).  One thread; the number of batches
+// is small.
+__device__ __forceinline__ int64_t batch_cost(const int64_t *word_off, const int64_t *qoff, int64_t b0, int64_t b1,
+                                              int64_t per_query)
+{
+    const int64_t dw = word_off[b1] - word_off[b0];
+    return dw + (dw >> 5) + 2 + per_query * (qoff[b1] - qoff[b0]);
+}
+
 __global__ void k_plan_batches(const int64_t *__restrict__ word_off, const int64_t *__restrict__ unit_off,
-                               const int64_t *__restrict__ qoff, int64_t T, int64_t cap_words,
+                               const int64_t *__restrict__ qoff, int64_t T, int64_t cap_words, int64_t per_query,
                                int64_t *__restrict__ boundaries, int64_t *__restrict__ info,
                                int64_t *__restrict__ nb_out, int *flags)
 {
@@ -356,15 +366,15 @@ __global__ void k_plan_batches(const int64_t *__restrict__ word_off, const int64
     int64_t nb = 0, start = 0;
     while (start < T) {
         boundaries[nb++] = start;
-        // largest end in (start, T] with word_off[end] - word_off[start] <= cap
+        // largest end in (start, T] whose cost fits in cap_words
         int64_t lo = start + 1, hi = T;
-        if (word_off[lo] - word_off[start] > cap_words) {
+        if (batch_cost(word_off, qoff, start, lo, per_query) > cap_words) {
             flags[kFlagPlanTooSmall] = 1;
             break;
         }
         while (lo < hi) {
             const int64_t mid = (lo + hi + 1) >> 1;
-            if (word_off[mid] - word_off[start] <= cap_words) lo = mid; else hi = mid - 1;
+            if (batch_cost(word_off, qoff, start, mid, per_query) <= cap_words) lo = mid; else hi = mid - 1;
         }
         start = lo;
     }
@@ -496,11 +506,11 @@ cudaError_t tile_fill(const uint32_t *order, const int32_t *cell_start, const in
 }
 
 cudaError_t plan_batches(const int64_t *tile_word_off, const int64_t *tile_unit, const int64_t *tile_qoff,
-                         int64_t T, int64_t cap_words, int64_t *boundaries, int64_t *info, int64_t *nb_out,
-                         int *flags, cudaStream_t s, int64_t *launches)
+                         int64_t T, int64_t cap_words, int64_t per_query_words, int64_t *boundaries, int64_t *info,
+                         int64_t *nb_out, int *flags, cudaStream_t s, int64_t *launches)
 {
-    k_plan_batches<<<1, 32, 0, s>>>(tile_word_off, tile_unit, tile_qoff, T, cap_words, boundaries, info, nb_out,
-                                    flags);
+    k_plan_batches<<<1, 32, 0, s>>>(tile_word_off, tile_unit, tile_qoff, T, cap_words, per_query_words, boundaries,
+                                    info, nb_out, flags);
     ++*launches;
     return cudaGetLastError();
 }

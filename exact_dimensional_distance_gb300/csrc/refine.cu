@@ -774,6 +774,10 @@ __global__ void __launch_bounds__(kCompactWarps * 32) k_compact(const CompactArg
             a.mask_row_ptr[gq] = woff;
             if (gq == a.nq - 1) a.mask_row_ptr[a.nq] = woff + W4;
         }
+        if (a.row_ptr_out) {
+            a.row_ptr_out[gq] = a.row_ptr[gq] - a.col0;
+            if (gq == a.nq - 1) a.row_ptr_out[a.nq] = a.row_ptr[a.nq] - a.col0;
+        }
     }
     if (!a.cols) return;
     const int ns = a.nbr_cnt[c];
@@ -795,7 +799,7 @@ __global__ void __launch_bounds__(kCompactWarps * 32) k_compact(const CompactArg
     // only the nonzero words of the row are visited: lane l takes occupancy
     // word o = o0 + 32 s + l (bits = mask words 32 o .. 32 o + 31), clipped to
     // the row's words [woff, woff + W)
-    int32_t *out = a.cols + a.row_ptr[gq];
+    int32_t *out = a.cols + (a.row_ptr[gq] - a.col0);
     int64_t run = 0;
     const int64_t o0 = woff >> 5, o1 = (woff + W - 1) >> 5;
     for (int64_t ob = o0; ob <= o1; ob += 32) {

@@ -134,7 +134,15 @@ typedef struct {
  * largest work goes first (RT-HiSS Section IV-D), and cuts them, one query
  * tile at a time, into batches whose result mask (one bit per candidate
  * pair, ceil(B_q / 32) words per query rounded up to a multiple of 4) fits
- * in batch_bytes.  Each batch is
+ * in three quarters of batch_bytes together with its occupancy bitmap (one
+ * bit per mask word) and its per-query arrays (counts, row offsets, ids; 24
+ * bytes per query, 40 with HISS_OUT_MASK, 44 for CSR copied to the host,
+ * whose batches alternate between two sets).  The CSR columns of a batch get
+ * the rest of batch_bytes (half of it per set when copied to the host); a
+ * batch whose result is larger is compacted and handed over in parts of
+ * consecutive queries, each a batch of its own for the callback, so the
+ * library's batch memory stays within batch_bytes.  HISS_E_BATCH_TOO_SMALL:
+ * one query tile, or one query's row of results, does not fit.  Each batch is
  * refined exactly on CUDA cores (float32 squared distances summed in
  * variance order, pair rejected once the partial sum exceeds eps^2; bit =
  * sum <= eps^2), compacted from the mask to CSR (Section IV-F1) unless
@@ -230,6 +238,8 @@ typedef struct {
     float eps;
     double cell_width;
     double ms_build, ms_index, ms_count, ms_refine, ms_compact, ms_deliver, ms_total;
+    int64_t deliveries;             /* batches handed to the callback: more than batches when a batch's
+                                       CSR result outgrew its share of batch_bytes and came in parts */
 } hiss_stats;
 
 int hiss_last_stats(const hiss_ctx *ctx, hiss_stats *out);

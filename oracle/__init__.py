@@ -17,7 +17,9 @@ Searches"):
   candidates (grid indexing of Section II-B1, with the Morton order of
   Section IV-C), written as numpy steps in the order the method takes them;
 * the count bound of the first intersection test (Section IV-D);
-* the stream compaction of the result mask (Section IV-F1, Fig. 5).
+* the stream compaction of the result mask (Section IV-F1, Fig. 5);
+* a per-row digest (count, splitmix64 fingerprint, boundary-band count) of
+  the join's rows, for comparing rows too large to list.
 
 The grid, Morton key and count-bound functions define one reading of the
 pages (the pages index with an RT-core BVH that this build replaces); each
@@ -63,6 +65,7 @@ def _lib():
         lib.orc_pick_eps2.argtypes = [p, i64, i32, p, i64, i64, i64, p, p]
         lib.orc_semi_count.argtypes = [p, i64, p, i64, i32, f64, f64, p]
         lib.orc_semi_fill.argtypes = [p, i64, p, i64, i32, f64, f64, p, p, p, p]
+        lib.orc_rows_digest.argtypes = [p, i64, i32, f64, f64, p, i64, p, p, p]
         lib.orc_pick_eps2.restype = ctypes.c_int
         _lib_handle = lib
     return _lib_handle
@@ -122,6 +125,21 @@ def rows(x, eps, query_rows, band: float = BAND):
     lib.orc_rows_fill(_ptr(x), x.shape[0], x.shape[1], e2, float(band), _ptr(q), q.size,
                       _ptr(row_ptr), _ptr(cols), _ptr(flag), _ptr(dist2))
     return row_ptr, cols[:nnz], flag[:nnz], dist2[:nnz]
+
+
+def rows_digest(x, eps, query_rows, band: float = BAND):
+    """Per query row i, without listing the pairs: (count, hash, band) with
+    count = |{j : s(i, j) <= eps^2}| (the definition, no band), hash = the sum
+    modulo 2^64 of splitmix64(j) over those j, and band = the number of j with
+    |s(i, j) - eps^2| <= band eps^2.  Used to compare large rows."""
+    x = _points(x)
+    q = np.ascontiguousarray(query_rows, dtype=np.int64)
+    cnt = np.empty(q.size, dtype=np.int64)
+    h = np.empty(q.size, dtype=np.uint64)
+    b = np.empty(q.size, dtype=np.int64)
+    _lib().orc_rows_digest(_ptr(x), x.shape[0], x.shape[1], eps_squared(eps), float(band), _ptr(q), q.size,
+                           _ptr(cnt), _ptr(h), _ptr(b))
+    return cnt, h, b
 
 
 def semi_rows(xq, xd, eps, band: float = BAND):

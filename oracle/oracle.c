@@ -85,6 +85,52 @@ void orc_rows_fill(const float *x, int64_t n, int32_t d, double eps2, double ban
 }
 
 /*
+ * splitmix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number
+ * generators", OOPSLA 2014; the 64-bit finaliser as published by Vigna): the
+ * first output of a generator seeded with v.  Used only to fingerprint
+ * neighbour sets, so that large rows can be compared without listing them.
+ */
+static uint64_t splitmix64(uint64_t v)
+{
+    uint64_t z = v + 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+/*
+ * A digest of each listed query row i = rows[r] of the definition's result
+ * (no band): out_count[r] = |{j : s(i,j) <= eps2}|, out_hash[r] = the sum,
+ * modulo 2^64, of splitmix64(j) over those j, and out_band[r] = the number of
+ * j with |s(i,j) - eps2| <= band * eps2 (pairs a correct float32
+ * implementation may decide either way).  One pass, nothing listed.
+ */
+void orc_rows_digest(const float *x, int64_t n, int32_t d, double eps2, double band,
+                     const int64_t *rows, int64_t nrows, int64_t *out_count, uint64_t *out_hash,
+                     int64_t *out_band)
+{
+    const double hi = eps2 * (1.0 + band);
+    const double lo = eps2 * (1.0 - band);
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t r = 0; r < nrows; ++r) {
+        const float *q = x + rows[r] * (int64_t)d;
+        int64_t c = 0, b = 0;
+        uint64_t h = 0;
+        for (int64_t j = 0; j < n; ++j) {
+            const double s = sqdist(q, x + j * (int64_t)d, d);
+            if (s <= eps2) {
+                ++c;
+                h += splitmix64((uint64_t)j);
+            }
+            if (s >= lo && s <= hi) ++b;
+        }
+        out_count[r] = c;
+        out_hash[r] = h;
+        out_band[r] = b;
+    }
+}
+
+/*
  * Semi-join (RT-HiSS Section II-A: "D and Q are distinct"): for each query
  * row r of xq (nq x d), count the points j of xd (nd x d) with
  * s(q_r, p_j) <= eps2 * (1 + band); then list them (increasing j) with the

@@ -39,8 +39,31 @@ def test_binding_names_match_header():
         assert callable(getattr(edd, name))
 
 
-def test_struct_sizes_match_header_layout():
+def test_struct_layouts_match_header(tmp_path):
+    # the binding's ctypes structures against the C compiler's layout of hiss.h
+    import shutil
+    import subprocess
+    import pytest
     import exact_dimensional_distance_gb300 as edd
-    # int64 x10, int32 x4, float, double x8 (with one 4-byte pad before the first double)
-    assert ctypes.sizeof(edd.hiss_stats) == 10 * 8 + 4 * 4 + 4 + 4 + 8 * 8
-    assert ctypes.sizeof(edd.hiss_batch) == 10 * 8 + 2 * 4
+    if shutil.which("gcc") is None:
+        pytest.skip("needs gcc")
+    structs = {"hiss_stats": edd.hiss_stats, "hiss_batch": edd.hiss_batch, "hiss_out": edd.hiss_out,
+               "hiss_index_view": edd.hiss_index_view}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "hiss.h"', "int main(void) {"]
+    for name, cls in structs.items():
+        lines.append('printf("%s size %%zu\\n", sizeof(%s));' % (name, name))
+        for field, _ in cls._fields_:
+            lines.append('printf("%s %s %%zu\\n", offsetof(%s, %s));' % (name, field, name, field))
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.check_call(["gcc", "-I" + os.path.join(ROOT, "include"), "-o", str(exe), str(src)])
+    got = {}
+    for line in subprocess.check_output([str(exe)], text=True).splitlines():
+        a, b, v = line.split()
+        got[(a, b)] = int(v)
+    for name, cls in structs.items():
+        assert got[(name, "size")] == ctypes.sizeof(cls), name
+        for field, _ in cls._fields_:
+            assert got[(name, field)] == getattr(cls, field).offset, (name, field)

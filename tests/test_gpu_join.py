@@ -186,6 +186,48 @@ def test_batching_matches_single_batch():
     _check_rows(x, eps, rows2, np.arange(0, len(x), 37))
 
 
+@pytest.mark.parametrize("copy_to_host", [False, True])
+def test_dense_result_comes_in_parts_within_batch_bytes(copy_to_host):
+    # eps covers every pair, so the CSR result (n^2 ids, 64 MB) is 32 times
+    # the result mask (2 MB).  With batch_bytes = 8 MB the mask fits in one
+    # batch but its CSR does not: the join must hand the batch over in parts
+    # that fit, and the context must stay under an allocation cap that the
+    # whole CSR would break, instead of failing with HISS_E_NOMEM.
+    edd = _edd()
+    x = datagen.generate(1, n=4000)          # U[0,1)^16: every distance < 4
+    n, eps = len(x), 10.0
+    j = edd.Join()
+    j.build(torch.from_numpy(x).cuda())
+    j.set_alloc_limit(40 << 20)
+    rows, nq_seen, idx = {}, [0], []
+
+    def take(b):
+        idx.append(int(b.index))
+        if copy_to_host:
+            q = edd._host_array(b.query_ids, b.nq, np.int64)
+            rp = edd._host_array(b.row_ptr, b.nq + 1, np.int64)
+            cols = edd._host_array(b.cols, b.nnz, np.int32)
+        else:
+            q = torch.as_tensor(edd.DeviceArray(b.query_ids, (b.nq,), "<i8"), device="cuda").cpu().numpy()
+            rp = torch.as_tensor(edd.DeviceArray(b.row_ptr, (b.nq + 1,), "<i8"), device="cuda").cpu().numpy()
+            cols = torch.as_tensor(edd.DeviceArray(b.cols, (b.nnz,), "<i4"), device="cuda").cpu().numpy()
+        assert rp[0] == 0 and rp[-1] == b.nnz and 4 * b.nnz <= 8 << 20
+        nq_seen[0] += b.nq
+        for i in range(b.nq):
+            assert int(q[i]) not in rows
+            rows[int(q[i])] = np.sort(cols[rp[i]:rp[i + 1]])
+
+    st = j.join(eps, 8 << 20, edd.HISS_OUT_CSR, copy_to_host, take)
+    j.close()
+    assert st["pairs"] == n * n
+    assert st["deliveries"] > st["batches"] >= 1
+    assert idx == list(range(st["deliveries"]))
+    assert nq_seen[0] == n and sorted(rows) == list(range(n))
+    everyone = np.arange(n)
+    for q in range(n):
+        assert np.array_equal(rows[q], everyone)
+
+
 def test_device_and_host_delivery_agree():
     edd = _edd()
     x = datagen.generate(3, n=4000)
@@ -230,7 +272,7 @@ def test_overlapped_host_delivery_many_batches_and_callback_stop():
             host[int(q[i])] = np.sort(cols[rp[i]:rp[i + 1]])
 
     st = j.join(eps, 1 << 16, edd.HISS_OUT_CSR, True, take)
-    assert st["batches"] >= 3 and order == list(range(st["batches"]))
+    assert st["batches"] >= 3 and order == list(range(st["deliveries"]))
     dev = j.join_sets(eps)  # one batch
     assert set(host) == set(dev) == set(range(len(x)))
     for q in range(len(x)):

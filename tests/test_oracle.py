@@ -266,6 +266,44 @@ def test_semi_join_hand_case():
     assert oracle.semi_brute_force_py(xq, xd, 5.0) == [{0, 1}, {1}, {2}, set()]
 
 
+def test_splitmix64_published_outputs():
+    from rowdigest import splitmix64
+    assert int(splitmix64(0)) == 0xE220A8397B1DCDAF                   # seed 0, first output
+    # seed 1234567: first and second outputs (the second is seeded one golden step on)
+    assert int(splitmix64(1234567)) == 6457827717110365317
+    assert int(splitmix64(1234567 + 0x9E3779B97F4A7C15)) == 3203168211198807973
+
+
+def test_rows_digest_hand_case():
+    from rowdigest import splitmix64
+    x = np.array([[0.0, 0.0], [3.0, 4.0], [10.0, 0.0]], dtype=np.float32)
+    c, h, b = oracle.rows_digest(x, 5.0, [0, 1, 2])
+    h01 = (int(splitmix64(0)) + int(splitmix64(1))) % (1 << 64)
+    assert c.tolist() == [2, 2, 1]
+    assert [int(v) for v in h] == [h01, h01, int(splitmix64(2))]
+    assert b.tolist() == [1, 1, 0]                     # the 3-4-5 pair sits exactly on eps
+    # eps one float32 step below 5: the pair is just outside eps, still in the band
+    c, h, b = oracle.rows_digest(x, float(np.nextafter(np.float32(5.0), np.float32(0.0))), [0, 1, 2])
+    assert c.tolist() == [1, 1, 1] and b.tolist() == [1, 1, 0]
+    assert [int(v) for v in h] == [int(splitmix64(0)), int(splitmix64(1)), int(splitmix64(2))]
+
+
+def test_rows_digest_matches_listed_rows():
+    from rowdigest import row_hash
+    x = datagen.generate(2, n=3000)
+    q = datagen.sample_queries(len(x), 200, seed=4)
+    eps = oracle.pick_eps(x, 20, q)["eps"]
+    c, h, b = oracle.rows_digest(x, eps, q)
+    row_ptr, cols, flag, dist2 = oracle.rows(x, eps, q)
+    e2 = oracle.eps_squared(eps)
+    for r in range(q.size):
+        sl = slice(row_ptr[r], row_ptr[r + 1])
+        inside = cols[sl][dist2[sl] <= e2]
+        assert c[r] == inside.size
+        assert int(h[r]) == row_hash(inside)
+        assert b[r] == int(flag[sl].sum())
+
+
 def semi_bound_hand_case():
     """The hand-computed semi-join count bounds of tests/golden/semi_bound_hand.txt."""
     g = read_golden("semi_bound_hand.txt")

@@ -28,6 +28,9 @@ MUTANTS = {
     "picker_keeps_self": ("if (j != i) buf[m++]", "buf[m++]"),
     "picker_off_by_one": ("const double a = pool[nq * K - 1], b = pool[nq * K];",
                           "const double a = pool[nq * K], b = pool[nq * K + 1];"),
+    "digest_hash_shifted_id": ("h += splitmix64((uint64_t)j);", "h += splitmix64((uint64_t)j + 1);"),
+    "digest_strict": ("if (s <= eps2) {", "if (s < eps2) {"),
+    "digest_band_one_sided": ("if (s >= lo && s <= hi) ++b;", "if (s >= lo && s <= eps2) ++b;"),
     "picker_never_retries": ("if (!(b < kth[r])) { status = 1; break; }", "if (0) { status = 1; break; }"),
 }
 
@@ -39,6 +42,7 @@ def _load(path):
     lib.orc_counts.argtypes = [p, i64, i32, f64, p]
     lib.orc_pick_eps2.argtypes = [p, i64, i32, p, i64, i64, i64, p, p]
     lib.orc_pick_eps2.restype = ctypes.c_int
+    lib.orc_rows_digest.argtypes = [p, i64, i32, f64, f64, p, i64, p, p, p]
     return lib
 
 
@@ -61,6 +65,22 @@ def _pin_cases():
 
 
 def _pins_hold(lib) -> bool:
+    # row digest: the 3-4-5 pair lies exactly on eps (inside, and in the band)
+    from rowdigest import splitmix64
+    x = np.array([[0.0, 0.0], [3.0, 4.0], [10.0, 0.0]], dtype=np.float32)
+    q = np.arange(3, dtype=np.int64)
+    c, h, b = np.empty(3, np.int64), np.empty(3, np.uint64), np.empty(3, np.int64)
+    lib.orc_rows_digest(x.ctypes.data, 3, 2, oracle.eps_squared(5.0), 1e-5, q.ctypes.data, 3, c.ctypes.data,
+                        h.ctypes.data, b.ctypes.data)
+    h01 = (int(splitmix64(0)) + int(splitmix64(1))) % (1 << 64)
+    if c.tolist() != [2, 2, 1] or [int(v) for v in h] != [h01, h01, int(splitmix64(2))] or b.tolist() != [1, 1, 0]:
+        return False
+    # eps one float32 step below 5: the pair is just outside, still in the band
+    e_lo = float(np.nextafter(np.float32(5.0), np.float32(0.0)))
+    lib.orc_rows_digest(x.ctypes.data, 3, 2, oracle.eps_squared(e_lo), 1e-5, q.ctypes.data, 3, c.ctypes.data,
+                        h.ctypes.data, b.ctypes.data)
+    if c.tolist() != [1, 1, 1] or b.tolist() != [1, 1, 0]:
+        return False
     for x, eps, want in _pin_cases():
         n, d = x.shape
         e2 = oracle.eps_squared(eps)
