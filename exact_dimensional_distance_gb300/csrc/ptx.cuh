@@ -40,6 +40,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
                  : "memory");
     return ok != 0;
 }
+// As mbar_try_wait, but a thread whose phase is not complete is suspended
+// (issuing nothing) until the phase completes or hint_ns nanoseconds pass,
+// instead of returning at once.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+                 : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ uint64_t global_ns()
 {
     uint64_t t;
@@ -63,6 +76,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
             if (abort && *abort) return false;
             if (global_ns() - t0 > kWaitLimitNs) return false;
         }
+    }
+}
+
+// A bounded wait whose thread sleeps in the barrier instead of polling: each
+// try suspends it until the phase completes (or kSuspendHintNs passes), so a
+// waiting warp takes no issue slots from the warps it waits for.  Gives up
+// (returns false) after kWaitLimitNs.
+constexpr uint32_t kSuspendHintNs = 1000000u;
+__device__ __forceinline__ bool mbar_wait_suspend(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
     }
 }
 

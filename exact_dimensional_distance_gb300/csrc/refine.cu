@@ -199,6 +199,21 @@ __device__ __forceinline__ void block_step2(f32x2 (&acc)[MQ / 2][MP], const floa
     }
 }
 
+// Minimum / maximum over the warp in one instruction (sm_100-family
+// redux.sync on float32; NaN-free inputs here).
+__device__ __forceinline__ float warp_min(float v)
+{
+    float r;
+    asm volatile("redux.sync.min.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+__device__ __forceinline__ float warp_max(float v)
+{
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
 __device__ __forceinline__ float min3(float a, float b, float c)
 {
     float r;
@@ -311,9 +326,18 @@ __device__ __forceinline__ void survivors(const f32x2 (&acc)[MQ / 2][MP], const 
 // check would end, so the first check comes later: after 6 dimensions at
 // d4 = 32 and 10 at d4 = 16 (gmm refinement 35.2 ms with the first check
 // after 2, 34.4 after 6; exp 15.3 s after 2, 14.7 s after 10).
+#ifndef HISS_FIRST_CHECK16
+#define HISS_FIRST_CHECK16 10
+#endif
+#ifndef HISS_FIRST_CHECK32
+#define HISS_FIRST_CHECK32 6
+#endif
+#ifndef HISS_FIRST_CHECK64
+#define HISS_FIRST_CHECK64 2
+#endif
 __host__ __device__ __forceinline__ constexpr int first_check(int d4)
 {
-    return d4 == 16 ? 10 : (d4 == 32 ? 6 : 2);
+    return d4 == 16 ? HISS_FIRST_CHECK16 : (d4 == 32 ? HISS_FIRST_CHECK32 : HISS_FIRST_CHECK64);
 }
 template <int MQ>
 __device__ __forceinline__ bool exit_check_at(int k, int d4)
@@ -321,13 +345,22 @@ __device__ __forceinline__ bool exit_check_at(int k, int d4)
     return MQ == 8 ? k >= first_check(d4) : (k & 3) == 0;
 }
 
-// Box test: used up to d4 = 32, where the ring has 6 stages.  The producer
-// waits for its coordinate loads before it can store a tile's boxes; with
-// the 2-stage rings of larger d4 that wait starves the compute warps
-// (subspace, d = 64: 2.78 -> 3.13 s; spectrum, d = 128: 0.52 -> 0.57 s).
-#ifndef HISS_BOX_MAXD4
-#define HISS_BOX_MAXD4 32
+
+// Stage waits sleep in the barrier (mbarrier.try_wait with a suspend-time
+// hint) rather than polling it, so that waiting warps (mostly the producer,
+// which runs ahead of the compute warps) leave the issue slots to the
+// arithmetic.  0: poll.
+#ifndef HISS_WAIT_SUSPEND
+#define HISS_WAIT_SUSPEND 1
 #endif
+__device__ __forceinline__ bool refine_wait(uint64_t *bar, uint32_t parity)
+{
+#if HISS_WAIT_SUSPEND
+    return mbar_wait_suspend(bar, parity);
+#else
+    return mbar_wait(bar, parity);
+#endif
+}
 
 // Resident blocks per SM the register budget is sized for.
 #ifndef HISS_REFINE_MINB
@@ -363,14 +396,9 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
     __shared__ int32_t s_nstart[kStencil];
     __shared__ int32_t s_vpre[kStencil + 1];
     __shared__ int64_t s_info[2];
-    // per stage and candidate half (32 rows, one compute warp's columns): the
-    // box of the staged candidates over the three index dimensions, lo at
-    // [0..2], hi at [4..6]
-    __shared__ __align__(16) float s_box[kMaxStages][kCandWarps][8];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d4 = D4 > 0 ? D4 : a.d4, S = tile_stride(d4), S2 = pair_stride(d4), C4 = d4 / 4;
-    const bool box = d4 <= HISS_BOX_MAXD4;  // box test over the three index dimensions
     const int nst = refine_stages<MQ, MP>(d4);
     float *Q2 = smem;
     float *P0 = smem + (kTQ / 2) * S2;
@@ -424,25 +452,21 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
         // ---- producer warp: stream the chunk through the stage ring ----
         // Each lane copies the 16-byte chunks of rows lane and lane + 32 of
         // a staged tile (cp.async), then arrives on the stage's full barrier
-        // twice: once asynchronously when its copies land, once now.  With
-        // the box test it first loads the rows' first 4 coordinates and
-        // stores the boxes of the tile's two halves.
+        // twice: once asynchronously when its copies land, once now.
         for (int it = 0; it < ntiles; ++it) {
             const int st = it % nst;
             const uint32_t round = (uint32_t)(it / nst);
-            if (it >= nst && !mbar_wait(&s_empty[st], (round - 1u) & 1u)) {
+            if (it >= nst && !refine_wait(&s_empty[st], (round - 1u) & 1u)) {
                 atomicExch(&a.flags[kFlagRefineTimeout], 1);
                 return;
             }
             float *P = P0 + st * kTP * S;
             const int64_t v0 = vbeg + (int64_t)it * kTP;
-            float4 head[kTP / 32];  // first 4 coordinates of rows lane, lane + 32 (none: +inf)
 #pragma unroll
             for (int h = 0; h < kTP / 32; ++h) {
                 const int r = lane + 32 * h;
                 const int64_t v = v0 + r;
                 float4 *row = reinterpret_cast<float4 *>(P + r * S);
-                head[h] = make_float4(INFINITY, INFINITY, INFINITY, INFINITY);
                 if (v < vend) {
                     int lo = 0, hi = ncell - 1;  // last slot with s_vpre[slot] <= v
                     while (lo < hi) {
@@ -450,38 +474,12 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
                         if (s_vpre[mid] <= v) lo = mid; else hi = mid - 1;
                     }
                     const float *src = a.xs + (int64_t)(s_nstart[lo] + (int32_t)(v - s_vpre[lo])) * d4;
-                    if (box) head[h] = __ldg(reinterpret_cast<const float4 *>(src));
                     for (int cc = 0; cc < C4; ++cc) cp_async16(row + cc, src + 4 * cc);
                 } else {
                     // no candidate: -inf makes every distance to this row +inf
                     for (int cc = 0; cc < C4; ++cc)
                         row[cc] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
                 }
-            }
-            if (box) {
-                // box of each half over the three index dimensions (rows past
-                // the chunk end are left out; an empty half gets lo = +inf,
-                // hi = -inf)
-#pragma unroll
-                for (int h = 0; h < kTP / 32; ++h) {
-                    const bool has = head[h].x != INFINITY;
-                    float l0 = head[h].x, l1 = head[h].y, l2 = head[h].z;
-                    float h0 = has ? l0 : -INFINITY, h1 = has ? l1 : -INFINITY, h2 = has ? l2 : -INFINITY;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        l0 = fminf(l0, __shfl_xor_sync(0xffffffffu, l0, o));
-                        l1 = fminf(l1, __shfl_xor_sync(0xffffffffu, l1, o));
-                        l2 = fminf(l2, __shfl_xor_sync(0xffffffffu, l2, o));
-                        h0 = fmaxf(h0, __shfl_xor_sync(0xffffffffu, h0, o));
-                        h1 = fmaxf(h1, __shfl_xor_sync(0xffffffffu, h1, o));
-                        h2 = fmaxf(h2, __shfl_xor_sync(0xffffffffu, h2, o));
-                    }
-                    if (lane == 0) {
-                        *reinterpret_cast<float4 *>(&s_box[st][h][0]) = make_float4(l0, l1, l2, 0.f);
-                        *reinterpret_cast<float4 *>(&s_box[st][h][4]) = make_float4(h0, h1, h2, 0.f);
-                    }
-                }
-                __syncwarp();
             }
             cp_async_arrive_on(&s_full[st]);
             mbar_arrive(&s_full[st]);
@@ -540,7 +538,7 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
     for (int it = 0; it < ntiles; ++it) {
         const int st = it % nst;
         const uint32_t round = (uint32_t)(it / nst);
-        if (!mbar_wait(&s_full[st], round & 1u)) {
+        if (!refine_wait(&s_full[st], round & 1u)) {
             atomicExch(&a.flags[kFlagRefineTimeout], 1);
             return;
         }
@@ -552,13 +550,17 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
         // e1 * e1 + s, e2 * e2 + s, so with rounding monotone G below is at
         // most each pair's float32 partial sum after 3 dimensions, which the
         // later terms only increase.  G > eps^2: every pair's bit is 0.
+        // The box of the warp's 32 staged candidates (rows 32 wp ...) is
+        // reduced from shared memory with single-instruction warp minima and
+        // maxima; rows past the chunk end hold -inf, which only widens it.
         bool far = false;
-        if (box) {
-            const float4 plo = *reinterpret_cast<const float4 *>(&s_box[st][wp][0]);
-            const float4 phi = *reinterpret_cast<const float4 *>(&s_box[st][wp][4]);
-            const float g0 = fmaxf(0.f, fmaxf(__fsub_rn(plo.x, qhi0), __fsub_rn(qlo0, phi.x)));
-            const float g1 = fmaxf(0.f, fmaxf(__fsub_rn(plo.y, qhi1), __fsub_rn(qlo1, phi.y)));
-            const float g2 = fmaxf(0.f, fmaxf(__fsub_rn(plo.z, qhi2), __fsub_rn(qlo2, phi.z)));
+        {
+            const float4 c = *reinterpret_cast<const float4 *>(P + (wp * 32 + lane) * S);
+            const float plo0 = warp_min(c.x), plo1 = warp_min(c.y), plo2 = warp_min(c.z);
+            const float phi0 = warp_max(c.x), phi1 = warp_max(c.y), phi2 = warp_max(c.z);
+            const float g0 = fmaxf(0.f, fmaxf(__fsub_rn(plo0, qhi0), __fsub_rn(qlo0, phi0)));
+            const float g1 = fmaxf(0.f, fmaxf(__fsub_rn(plo1, qhi1), __fsub_rn(qlo1, phi1)));
+            const float g2 = fmaxf(0.f, fmaxf(__fsub_rn(plo2, qhi2), __fsub_rn(qlo2, phi2)));
             far = __fmaf_rn(g2, g2, __fmaf_rn(g1, g1, __fmul_rn(g0, g0))) > eps2;
         }
         f32x2 acc[MQ / 2][MP];

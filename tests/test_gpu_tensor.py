@@ -101,7 +101,7 @@ def test_many_batches_and_duplicates_tensor():
     x = datagen.generate(1, n=4000)
     x[100:140] = x[7]
     eps = golden_eps(1)
-    rows, counts, st = _join(x, eps, batch_bytes=1 << 16)
+    rows, counts, st = _join(x, eps, batch_bytes=1 << 17)
     assert st["batches"] > 1
     _check_rows(x, eps, rows)
     rows0, _, _ = _join(x, 0.0)
