@@ -60,55 +60,99 @@ struct Geo {
 #endif
 constexpr int kMaxStages = HISS_REFINE_STAGES;
 
-// Stages of the candidate ring: as many as fit (up to 6, at least 2) in
-// about a third of the SM's shared memory, so that two or three blocks stay
-// resident per SM.
-template <int MQ, int MP>
-__host__ __device__ __forceinline__ int refine_stages(int d4)
+// Dimensions of each candidate row that the ring stages: all of them up to
+// HISS_STAGE_DIMS, else the first HISS_STAGE_DIMS.  Most pairs leave within
+// the first few dimensions (variance order), so staging whole rows of 64 or
+// 128 dimensions would fill the ring with data that is never read and leave
+// room for only two stages; the few pairs still within eps^2 after the staged
+// dimensions read the rest of their candidate's row from global memory (see
+// finish_pairs).  The work-profile build stages every dimension.
+// Measured on GB300: 64-dimensional subspace data 2.73 s with 32 dimensions
+// staged, 2.62 s with 16 (six stages instead of four); 128-dimensional
+// spectrum data 0.38 s with 32, 0.49 s with 16.
+#ifndef HISS_STAGE_DIMS
+#define HISS_STAGE_DIMS 32
+#endif
+#ifndef HISS_STAGE_DIMS64
+#define HISS_STAGE_DIMS64 16
+#endif
+template <bool PROF>
+__host__ __device__ __forceinline__ constexpr int staged_dims(int d4)
 {
-    const int q2 = (Geo<MQ, MP>::TQ / 2) * pair_stride(d4) * 4, stage = Geo<MQ, MP>::TP * tile_stride(d4) * 4;
-    int ns = (75 * 1024 - q2) / stage;
-    return ns < 2 ? 2 : (ns > kMaxStages ? kMaxStages : ns);
+    return (PROF || d4 <= 32) ? d4 : (d4 <= 64 ? HISS_STAGE_DIMS64 : HISS_STAGE_DIMS);
 }
+
 // Survivor mode.  A warp still in a tile after surv_dim dimensions counts its
 // pairs whose partial sum is still <= eps^2; if there are at most kSurvMax
 // of them and at least 8 dimensions are left, it stops the blocked
 // arithmetic and finishes those pairs one per lane, continuing each pair's
 // own float32 sum in dimension order (the same subtract and multiply-add, so
-// the same sums and bits), with a per-pair exit every 4 dimensions.  It is
-// used with 4 x 4 blocks (d4 > 64) and with 8 x 4 blocks at d4 = 64.  With
-// fewer dimensions the one-pair-per-lane path (2 scalar instructions and
-// about 0.75 shared loads per pair-dimension, against 1 packed instruction in
-// a register block) costs more than the blocked dimensions it saves.  The
-// lists sit in dynamic shared memory after the ring, only in builds that use
-// them.
+// the same sums and bits), with a per-pair exit.  A warp still in a tile when
+// the staged dimensions run out finishes all of its live pairs that way,
+// kSurvMax at a time.  The early switch is used with 4 x 4 blocks (d4 > 64)
+// and with 8 x 4 blocks at d4 = 64.  With fewer dimensions the
+// one-pair-per-lane path (2 scalar instructions and about 0.75 shared loads
+// per pair-dimension, against 1 packed instruction in a register block) costs
+// more than the blocked dimensions it saves.  The lists sit in dynamic shared
+// memory after the ring, only in builds that use them.
 #ifndef HISS_SURV8_DIM
 #define HISS_SURV8_DIM 16
 #endif
 #ifndef HISS_SURV4_DIM
-#define HISS_SURV4_DIM 48
+#define HISS_SURV4_DIM 16
 #endif
-constexpr int kSurvMax = 64;  // survivors a warp takes (a multiple of 32)
+constexpr int kSurvMax = 64;  // survivors a warp takes at a time (a multiple of 32)
+// 16-byte chunks of a candidate row a survivor loads from global memory at
+// once (its latency is paid once per chunk group)
+#ifndef HISS_SURV_AHEAD
+#define HISS_SURV_AHEAD 4
+#endif
+constexpr int kSurvAhead = HISS_SURV_AHEAD;
 // Dimension after which a warp may switch to survivor mode (a multiple of 4),
 // 0 for none.
 __host__ __device__ __forceinline__ constexpr int surv_dim(int mq, int d4)
 {
     return mq == 4 ? HISS_SURV4_DIM : (d4 == 64 ? HISS_SURV8_DIM : 0);
 }
+template <bool PROF>
+__host__ __device__ __forceinline__ constexpr bool uses_survivors(int mq, int d4)
+{
+    return surv_dim(mq, d4) > 0 || staged_dims<PROF>(d4) < d4;
+}
+template <bool PROF>
 __host__ __device__ __forceinline__ constexpr size_t surv_bytes(int mq, int d4)
 {
     // per compute warp: kSurvMax partial sums (float) and pair codes (uint16),
     // and 32 mask words
-    return surv_dim(mq, d4) > 0 ? (size_t)kComputeWarps * (kSurvMax * 6 + 32 * 4) : 0;
+    return uses_survivors<PROF>(mq, d4) ? (size_t)kComputeWarps * (kSurvMax * 6 + 32 * 4) : 0;
 }
 
-template <int MQ, int MP>
+// Bytes of one ring stage: the staged rows, then (when rows are staged
+// partly) the global row index of each staged candidate.
+template <int MQ, int MP, bool PROF>
+__host__ __device__ __forceinline__ int stage_bytes(int d4)
+{
+    const int ds = staged_dims<PROF>(d4);
+    return Geo<MQ, MP>::TP * (tile_stride(ds) * 4 + (ds < d4 ? 4 : 0));
+}
+
+// Stages of the candidate ring: as many as fit (up to 6, at least 2) in
+// about a third of the SM's shared memory, so that two or three blocks stay
+// resident per SM.
+template <int MQ, int MP, bool PROF>
+__host__ __device__ __forceinline__ int refine_stages(int d4)
+{
+    const int q2 = (Geo<MQ, MP>::TQ / 2) * pair_stride(d4) * 4 + (int)surv_bytes<PROF>(MQ, d4);
+    int ns = (75 * 1024 - q2) / stage_bytes<MQ, MP, PROF>(d4);
+    return ns < 2 ? 2 : (ns > kMaxStages ? kMaxStages : ns);
+}
+
+template <int MQ, int MP, bool PROF>
 __host__ __forceinline__ size_t refine_smem(int d4)
 {
     using G = Geo<MQ, MP>;
-    return sizeof(float) *
-               ((size_t)(G::TQ / 2) * pair_stride(d4) + (size_t)refine_stages<MQ, MP>(d4) * G::TP * tile_stride(d4)) +
-           surv_bytes(MQ, d4);
+    return sizeof(float) * (size_t)(G::TQ / 2) * pair_stride(d4) +
+           (size_t)refine_stages<MQ, MP, PROF>(d4) * stage_bytes<MQ, MP, PROF>(d4) + surv_bytes<PROF>(MQ, d4);
 }
 
 // Packed float32 pairs (two lanes of one 64-bit register), computed with the
@@ -257,47 +301,77 @@ __device__ __forceinline__ float block_min(const f32x2 (&acc)[MQ / 2][MP])
     return v[0];
 }
 
-// Survivor mode of one warp at dimension k: the pairs of its MQ x MP blocks
-// whose partial sum is still <= eps^2 (at most kSurvMax over the warp) are
-// listed in shared memory (query row << 5 | candidate column within the warp
-// tile, and the partial sum), then finished one per lane: dimensions k, k+1,
-// ... are added to the pair's own partial sum with the blocked path's
-// round-to-nearest subtract and fused multiply-add, in the same order, so the
-// final sum and bit are those of the blocked path.  A pair stops once its sum
-// exceeds eps^2 (checked every 4 dimensions).  The bits of the pairs within
-// eps^2 are gathered in sword[query row of the warp tile] (bit = candidate
-// column), ready for the caller after the closing __syncwarp.
+// Rank of this thread's first live pair among the warp's (exclusive prefix
+// of the per-thread counts of partial sums <= eps^2) and the warp's total.
 template <int MQ, int MP>
-__device__ __forceinline__ void survivors(const f32x2 (&acc)[MQ / 2][MP], const float *Q2, const float *P, int S2,
-                                          int S, int k, int d4, float eps2, int first, int total, int lane, int wq,
-                                          int wp, float *spart, uint16_t *sidx, uint32_t *sword)
+__device__ __forceinline__ void live_scan(const f32x2 (&acc)[MQ / 2][MP], float eps2, int lane, int *first,
+                                          int *total)
 {
-    const int lq = lane >> 3, lp = lane & 7;
-    int pos = first;
+    int live = 0;
 #pragma unroll
     for (int i = 0; i < MQ; ++i)
 #pragma unroll
-        for (int j = 0; j < MP; ++j) {
-            const float v = acc_at<MQ, MP>(acc, i, j);
-            if (v <= eps2) {
-                sidx[pos] = (uint16_t)(((lq + 4 * i) << 5) | (lp + 8 * j));
-                spart[pos] = v;
-                ++pos;
-            }
-        }
+        for (int j = 0; j < MP; ++j) live += (acc_at<MQ, MP>(acc, i, j) <= eps2) ? 1 : 0;
+    int incl = live;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    *first = incl - live;
+    *total = __shfl_sync(0xffffffffu, incl, 31);
+}
+
+// Survivor mode of one warp at dimension k: the pairs of its MQ x MP blocks
+// whose partial sum is still <= eps^2 (total of them over the warp; this
+// thread's rank from first) are listed in shared memory, kSurvMax at a time
+// (query row << 5 | candidate column within the warp tile, and the partial
+// sum), then finished one per lane: dimensions k, k+1, ... are added to the
+// pair's own partial sum with the blocked path's round-to-nearest subtract
+// and fused multiply-add, in the same order, so the final sum and bit are
+// those of the blocked path.  Dimensions below ds come from the staged tile
+// P; the rest from the candidate's row in global memory (xs, row srow[column],
+// 16 dimensions loaded ahead).  A pair stops once its sum exceeds eps^2.  The
+// bits of the pairs within eps^2 are gathered in sword[query row of the warp
+// tile] (bit = candidate column), ready for the caller after the closing
+// __syncwarp.
+template <int MQ, int MP>
+__device__ __forceinline__ void survivors(const f32x2 (&acc)[MQ / 2][MP], const float *Q2, const float *P,
+                                          const float *xs, const int32_t *srow, int S2, int S, int k, int ds, int d4,
+                                          float eps2, int first, int total, int lane, int wq, int wp, float *spart,
+                                          uint16_t *sidx, uint32_t *sword)
+{
+    const int lq = lane >> 3, lp = lane & 7;
     sword[lane] = 0u;
-    __syncwarp();
-    for (int e0 = 0; e0 < total; e0 += 32) {
-        const int e = e0 + lane;
-        if (e < total) {
+    for (int b0 = 0; b0 < total; b0 += kSurvMax) {
+        __syncwarp();
+        int pos = first;
+#pragma unroll
+        for (int i = 0; i < MQ; ++i)
+#pragma unroll
+            for (int j = 0; j < MP; ++j) {
+                const float v = acc_at<MQ, MP>(acc, i, j);
+                if (v <= eps2) {
+                    if (pos >= b0 && pos < b0 + kSurvMax) {
+                        sidx[pos - b0] = (uint16_t)(((lq + 4 * i) << 5) | (lp + 8 * j));
+                        spart[pos - b0] = v;
+                    }
+                    ++pos;
+                }
+            }
+        __syncwarp();
+        const int cnt = min(kSurvMax, total - b0);
+        for (int e = lane; e < cnt; e += 32) {
             const int code = sidx[e];
             const int r = code >> 5, pc = code & 31;
             const int qt = wq * (4 * MQ) + r;  // query row of the tile
             const float *qrow = Q2 + (4 * (qt >> 3) + (qt & 3)) * S2;
             const bool hi = ((qt >> 2) & 1) != 0;  // second row of its pair row
-            const float *prow = P + (wp * (8 * MP) + pc) * S;
+            const int prow_i = wp * (8 * MP) + pc;
+            const float *prow = P + prow_i * S;
             float sum = spart[e];
-            for (int kk = k; kk < d4; kk += 4) {
+            int kk = k;
+            for (; kk < ds; kk += 4) {
                 const float4 qa = *reinterpret_cast<const float4 *>(qrow + 2 * kk);
                 const float4 qb = *reinterpret_cast<const float4 *>(qrow + 2 * kk + 4);
                 const float4 pv = *reinterpret_cast<const float4 *>(prow + kk);
@@ -311,6 +385,36 @@ __device__ __forceinline__ void survivors(const f32x2 (&acc)[MQ / 2][MP], const 
                 df = __fsub_rn(hi ? qb.w : qb.z, pv.w);
                 sum = __fmaf_rn(df, df, sum);
                 if (sum > eps2) break;
+            }
+            if (sum <= eps2 && kk < d4) {
+                // dimensions past the staged ones, from the candidate's row
+                // (a live pair's candidate is a real row: padding rows are at
+                // +inf distance)
+                const float4 *pg = reinterpret_cast<const float4 *>(xs + (int64_t)srow[prow_i] * d4);
+                for (; kk < d4; kk += 4 * kSurvAhead) {
+                    float4 pv[kSurvAhead];
+#pragma unroll
+                    for (int u = 0; u < kSurvAhead; ++u)
+                        if (kk + 4 * u < d4) pv[u] = __ldg(pg + (kk >> 2) + u);
+#pragma unroll
+                    for (int u = 0; u < kSurvAhead; ++u) {
+                        const int k4 = kk + 4 * u;
+                        if (k4 < d4) {
+                            const float4 qa = *reinterpret_cast<const float4 *>(qrow + 2 * k4);
+                            const float4 qb = *reinterpret_cast<const float4 *>(qrow + 2 * k4 + 4);
+                            float df;
+                            df = __fsub_rn(hi ? qa.y : qa.x, pv[u].x);
+                            sum = __fmaf_rn(df, df, sum);
+                            df = __fsub_rn(hi ? qa.w : qa.z, pv[u].y);
+                            sum = __fmaf_rn(df, df, sum);
+                            df = __fsub_rn(hi ? qb.y : qb.x, pv[u].z);
+                            sum = __fmaf_rn(df, df, sum);
+                            df = __fsub_rn(hi ? qb.w : qb.z, pv[u].w);
+                            sum = __fmaf_rn(df, df, sum);
+                        }
+                    }
+                    if (sum > eps2) break;
+                }
             }
             if (sum <= eps2) atomicOr(&sword[r], 1u << pc);
         }
@@ -398,12 +502,17 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
     __shared__ int64_t s_info[2];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int d4 = D4 > 0 ? D4 : a.d4, S = tile_stride(d4), S2 = pair_stride(d4), C4 = d4 / 4;
-    const int nst = refine_stages<MQ, MP>(d4);
+    const int d4 = D4 > 0 ? D4 : a.d4, S2 = pair_stride(d4);
+    // staged dimensions per candidate row, their row stride and 16-byte chunks
+    const int ds = staged_dims<PROF>(d4), S = tile_stride(ds), C4 = ds / 4;
+    const bool partial_rows = ds < d4;
+    const int nst = refine_stages<MQ, MP, PROF>(d4);
     float *Q2 = smem;
     float *P0 = smem + (kTQ / 2) * S2;
-    // survivor lists (MQ == 4) after the stage ring
-    float *s_spart = P0 + nst * kTP * S;
+    // with partly staged rows: the global row of each staged candidate, per stage
+    int32_t *s_row = reinterpret_cast<int32_t *>(P0 + nst * kTP * S);
+    // survivor lists after the stage ring
+    float *s_spart = reinterpret_cast<float *>(s_row + (partial_rows ? nst * kTP : 0));
     uint16_t *s_sidx = reinterpret_cast<uint16_t *>(s_spart + kComputeWarps * kSurvMax);
     uint32_t *s_sword = reinterpret_cast<uint32_t *>(s_sidx + kComputeWarps * kSurvMax);
 
@@ -450,9 +559,11 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
 
     if (warp == kComputeWarps) {
         // ---- producer warp: stream the chunk through the stage ring ----
-        // Each lane copies the 16-byte chunks of rows lane and lane + 32 of
-        // a staged tile (cp.async), then arrives on the stage's full barrier
-        // twice: once asynchronously when its copies land, once now.
+        // Each lane copies the 16-byte chunks of the staged dimensions of
+        // rows lane and lane + 32 of a tile (cp.async), then arrives on the
+        // stage's full barrier twice: once asynchronously when its copies
+        // land, once now.  With partly staged rows it also records each
+        // row's index (-1 past the chunk end).
         for (int it = 0; it < ntiles; ++it) {
             const int st = it % nst;
             const uint32_t round = (uint32_t)(it / nst);
@@ -473,12 +584,15 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
                         const int mid = (lo + hi + 1) >> 1;
                         if (s_vpre[mid] <= v) lo = mid; else hi = mid - 1;
                     }
-                    const float *src = a.xs + (int64_t)(s_nstart[lo] + (int32_t)(v - s_vpre[lo])) * d4;
+                    const int32_t grow = s_nstart[lo] + (int32_t)(v - s_vpre[lo]);
+                    const float *src = a.xs + (int64_t)grow * d4;
                     for (int cc = 0; cc < C4; ++cc) cp_async16(row + cc, src + 4 * cc);
+                    if (partial_rows) s_row[st * kTP + r] = grow;
                 } else {
                     // no candidate: -inf makes every distance to this row +inf
                     for (int cc = 0; cc < C4; ++cc)
                         row[cc] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                    if (partial_rows) s_row[st * kTP + r] = -1;
                 }
             }
             cp_async_arrive_on(&s_full[st]);
@@ -490,8 +604,9 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
     // ---- compute warps ----
     // query tile, pair-interleaved: pair row pid holds rows a = 8 (pid / 4) +
     // pid % 4 and a + 4, dimension by dimension; rows >= nq are +inf
-    for (int idx = tid; idx < (kTQ / 2) * C4; idx += kComputeThreads) {
-        const int pid = idx / C4, cc = idx - pid * C4;
+    const int Q4 = d4 / 4;  // the query tile holds every dimension
+    for (int idx = tid; idx < (kTQ / 2) * Q4; idx += kComputeThreads) {
+        const int pid = idx / Q4, cc = idx - pid * Q4;
         const int ra = 8 * (pid >> 2) + (pid & 3), rb = ra + 4;
         const float4 inf4 = make_float4(INFINITY, INFINITY, INFINITY, INFINITY);
         const float4 x = ra < nq ? *reinterpret_cast<const float4 *>(a.xq + (int64_t)(q0 + ra) * d4 + 4 * cc) : inf4;
@@ -577,6 +692,9 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
                 for (int j = 0; j < MP; ++j) valid += (qbase + 4 * i < nq && v0 + pbase + 8 * j < vend) ? 1 : 0;
             prof_alg += (uint64_t)valid * (uint64_t)min(4, a.d);
             if (warp_live) prof_exec += (uint64_t)valid * (uint64_t)min(2, a.d);
+            // dimensions the timed kernel stages: a warp still live there
+            // finishes its pairs one per lane
+            const int dsk = staged_dims<false>(d4);
             int live = 0;
             for (int k = 2; k < d4; k += 2) {
                 if (warp_live && !surv && exit_check_at<MQ>(k, d4) &&
@@ -588,8 +706,10 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
                     for (int i = 0; i < MQ; ++i)
 #pragma unroll
                         for (int j = 0; j < MP; ++j) live += (acc_at<MQ, MP>(acc, i, j) <= eps2) ? 1 : 0;
-                    if (warp_live && !surv && k == surv_dim(MQ, d4) && d4 - k >= 8 &&
-                        __reduce_add_sync(0xffffffffu, live) <= kSurvMax)
+                    if (warp_live && !surv &&
+                        ((k == surv_dim(MQ, d4) && k < dsk && d4 - k >= 8 &&
+                          __reduce_add_sync(0xffffffffu, live) <= kSurvMax) ||
+                         k == dsk))
                         surv = true;  // survivor mode: each live pair runs on alone
                     if (!__any_sync(0xffffffffu, live > 0) && (!warp_live || surv)) break;
                     prof_alg += (uint64_t)live * (uint64_t)min(4, a.d - k);
@@ -603,11 +723,22 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
             // warp-level early termination (the pairs are in variance order,
             // most leave early)
             bool any_close = true, surv = false;
+            // A warp still live when the staged dimensions run out finishes
+            // its pairs one per lane (the rest of each candidate row comes
+            // from global memory); with whole rows staged that point is d4,
+            // where the bits are read from the sums.
+            int sk = 0, sfirst = 0, stotal = 0;  // survivor mode from dimension sk
             if constexpr (MQ == 8) {
                 // a check after every 2 dimensions
                 for (int k = 2;; k += 2) {
-                    if (k == d4) {
-                        any_close = __any_sync(0xffffffffu, block_min<MQ, MP>(acc) <= eps2);
+                    if (k == ds) {
+                        if (ds == d4) {
+                            any_close = __any_sync(0xffffffffu, block_min<MQ, MP>(acc) <= eps2);
+                        } else {
+                            live_scan<MQ, MP>(acc, eps2, lane, &sfirst, &stotal);
+                            any_close = surv = stotal > 0;
+                            sk = k;
+                        }
                         break;
                     }
                     if (exit_check_at<MQ>(k, d4) && __all_sync(0xffffffffu, block_min<MQ, MP>(acc) > eps2)) {
@@ -615,23 +746,10 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
                         break;
                     }
                     if (k == surv_dim(MQ, d4) && d4 - k >= 8) {
-                        int live = 0;
-#pragma unroll
-                        for (int i = 0; i < MQ; ++i)
-#pragma unroll
-                            for (int j = 0; j < MP; ++j) live += (acc_at<MQ, MP>(acc, i, j) <= eps2) ? 1 : 0;
-                        int incl = live;
-#pragma unroll
-                        for (int o = 1; o < 32; o <<= 1) {
-                            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-                            if (lane >= o) incl += v;
-                        }
-                        const int total = __shfl_sync(0xffffffffu, incl, 31);
-                        if (total <= kSurvMax) {
+                        live_scan<MQ, MP>(acc, eps2, lane, &sfirst, &stotal);
+                        if (stotal <= kSurvMax) {
                             surv = true;
-                            survivors<MQ, MP>(acc, Q2, P, S2, S, k, d4, eps2, incl - live, total, lane, wq, wp,
-                                              s_spart + warp * kSurvMax, s_sidx + warp * kSurvMax,
-                                              s_sword + warp * 32);
+                            sk = k;
                             break;
                         }
                     }
@@ -642,8 +760,14 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
                 // let the compiler overlap one step's loads with the other
                 block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, 2);
                 for (int k = 4;; k += 4) {
-                    if (k == d4) {
-                        any_close = __any_sync(0xffffffffu, block_min<MQ, MP>(acc) <= eps2);
+                    if (k == ds) {
+                        if (ds == d4) {
+                            any_close = __any_sync(0xffffffffu, block_min<MQ, MP>(acc) <= eps2);
+                        } else {
+                            live_scan<MQ, MP>(acc, eps2, lane, &sfirst, &stotal);
+                            any_close = surv = stotal > 0;
+                            sk = k;
+                        }
                         break;
                     }
                     if (__all_sync(0xffffffffu, block_min<MQ, MP>(acc) > eps2)) {
@@ -651,23 +775,10 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
                         break;
                     }
                     if (k == surv_dim(MQ, d4) && d4 - k >= 8) {
-                        int live = 0;
-#pragma unroll
-                        for (int i = 0; i < MQ; ++i)
-#pragma unroll
-                            for (int j = 0; j < MP; ++j) live += (acc_at<MQ, MP>(acc, i, j) <= eps2) ? 1 : 0;
-                        int incl = live;
-#pragma unroll
-                        for (int o = 1; o < 32; o <<= 1) {
-                            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-                            if (lane >= o) incl += v;
-                        }
-                        const int total = __shfl_sync(0xffffffffu, incl, 31);
-                        if (total <= kSurvMax) {
+                        live_scan<MQ, MP>(acc, eps2, lane, &sfirst, &stotal);
+                        if (stotal <= kSurvMax) {
                             surv = true;
-                            survivors<MQ, MP>(acc, Q2, P, S2, S, k, d4, eps2, incl - live, total, lane, wq, wp,
-                                              s_spart + warp * kSurvMax, s_sidx + warp * kSurvMax,
-                                              s_sword + warp * 32);
+                            sk = k;
                             break;
                         }
                     }
@@ -675,6 +786,9 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
                     block_step2<MQ, MP, false>(acc, Q2, P, S2, S, pidbase, pbase, k + 2);
                 }
             }
+            if (uses_survivors<false>(MQ, d4) && surv)
+                survivors<MQ, MP>(acc, Q2, P, a.xs, s_row + st * kTP, S2, S, sk, ds, d4, eps2, sfirst, stotal, lane,
+                                  wq, wp, s_spart + warp * kSurvMax, s_sidx + warp * kSurvMax, s_sword + warp * 32);
             // one bit per pair.  The warp's 32 candidate columns (pbase + 8 j)
             // form one mask word per query row: bit lp + 8 j.  A ballot per
             // (i, j) gives, for each lq, byte lq = the 8 lanes' bits; three
@@ -732,7 +846,7 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
 template <int MQ, int MP, bool PROF, int D4 = 0>
 cudaError_t launch_refine(const RefineArgs &a, cudaStream_t s)
 {
-    const size_t smem = refine_smem<MQ, MP>(a.d4);
+    const size_t smem = refine_smem<MQ, MP, PROF>(a.d4);
     static size_t configured = 0;  // largest dynamic shared memory requested so far
     if (smem > configured) {
         HISS_TRY(cudaFuncSetAttribute(k_refine<MQ, MP, PROF, D4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
