@@ -121,6 +121,27 @@ struct RefineArgs {
 };
 int refine_tq(int d4);
 int refine_chunk(int d4);
+// The float32 squared distance of two rows of d4 values (variance order,
+// padded) with the refinement's own arithmetic (the first product, then a
+// fused multiply-add per dimension, in dimension order), so that values
+// recomputed elsewhere (tensor-core recheck, kNN ranking) agree with its bits.
+__device__ __forceinline__ float refine_dist2(const float *q, const float *p, int d4)
+{
+    float s = 0.0f;
+    for (int k = 0; k < d4; k += 4) {
+        const float4 a = *reinterpret_cast<const float4 *>(q + k);
+        const float4 b = *reinterpret_cast<const float4 *>(p + k);
+        float e = __fsub_rn(a.x, b.x);
+        s = k == 0 ? __fmul_rn(e, e) : __fmaf_rn(e, e, s);
+        e = __fsub_rn(a.y, b.y);
+        s = __fmaf_rn(e, e, s);
+        e = __fsub_rn(a.z, b.z);
+        s = __fmaf_rn(e, e, s);
+        e = __fsub_rn(a.w, b.w);
+        s = __fmaf_rn(e, e, s);
+    }
+    return s;
+}
 cudaError_t refine(const RefineArgs &a, cudaStream_t s, int64_t *launches);
 cudaError_t refine_profile(const RefineArgs &a, cudaStream_t s, int64_t *launches);
 

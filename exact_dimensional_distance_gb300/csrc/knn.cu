@@ -4,8 +4,7 @@
 // has at least k neighbours within eps.
 //
 // Per batch: the squared distance of every (query, neighbour) pair is
-// recomputed in float32, summed in variance order (the arithmetic of the
-// refinement); pairs are ordered by neighbour id, then stably by (query,
+// recomputed in float32 with the refinement's arithmetic (refine_dist2); pairs are ordered by neighbour id, then stably by (query,
 // squared distance) with the library's radix sort, so each query's pairs end
 // up by increasing distance, equal distances by increasing id; the first k of
 // each query with at least k pairs are its result.
@@ -28,20 +27,7 @@ __global__ void __launch_bounds__(kKnnWarps * 32) k_knn_pairs(KnnBatchArgs a)
     for (int64_t p = p0 + lane; p < p1; p += 32) {
         const int32_t c = a.cols[a.pair0 + p];
         const float *x = a.xv + (int64_t)c * a.d4;
-        float s = 0.0f;
-        for (int k = 0; k < a.d4; k += 4) {
-            const float4 u = *reinterpret_cast<const float4 *>(q + k);
-            const float4 v = *reinterpret_cast<const float4 *>(x + k);
-            float e = u.x - v.x;
-            s = k == 0 ? e * e : fmaf(e, e, s);
-            e = u.y - v.y;
-            s = fmaf(e, e, s);
-            e = u.z - v.z;
-            s = fmaf(e, e, s);
-            e = u.w - v.w;
-            s = fmaf(e, e, s);
-        }
-        a.d2[p] = s;
+        a.d2[p] = refine_dist2(q, x, a.d4);
         a.prow[p] = (int32_t)r;
         a.keys[p] = (uint64_t)(uint32_t)c;
         a.vals[p] = (uint32_t)p;

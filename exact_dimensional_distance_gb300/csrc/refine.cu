@@ -47,6 +47,7 @@ constexpr int kRefineThreads = kComputeThreads + 32;
 #define HISS_REFINE_CHUNK 8192
 #endif
 constexpr int kCH = HISS_REFINE_CHUNK;  // candidates per unit (a multiple of 64)
+__host__ __device__ __forceinline__ int refine_chunk_of(int) { return kCH; }
 
 // Per-thread block MQ x MP: 8 x 4 up to d4 = 64 (tiles of 128 queries x 64
 // candidates), 4 x 4 above (64 x 64), so that two blocks fit per SM.
@@ -472,6 +473,113 @@ __device__ __forceinline__ bool refine_wait(uint64_t *bar, uint32_t parity)
 #endif
 
 
+// Per-unit state of a refinement block.
+struct Unit {
+    int64_t t;           // query tile
+    int64_t B, W, W4;    // candidates of the tile's cell, meaningful mask words per row, row stride
+    int64_t vbeg, vend;  // this unit's chunk of the cell's concatenated stencil
+    int32_t c, q0;       // cell, first query row
+    int nq, ncell, ntiles;
+};
+
+// Finds the block's unit (the last query tile whose first unit is at most
+// the block's), initialises the stage barriers and the stencil's cell
+// offsets.  All threads of the block call it.
+template <int TP>
+__device__ __forceinline__ Unit unit_begin(const RefineArgs &a, int nst, uint64_t *s_full, uint64_t *s_empty,
+                                           int32_t *s_nstart, int32_t *s_vpre, int64_t *s_info)
+{
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        const int64_t u = a.unit0 + blockIdx.x;
+        int64_t lo = a.t0, hi = a.t1 - 1;  // last tile with tile_unit[t] <= u
+        while (lo < hi) {
+            const int64_t mid = (lo + hi + 1) >> 1;
+            if (a.tile_unit[mid] <= u) lo = mid; else hi = mid - 1;
+        }
+        s_info[0] = lo;
+        s_info[1] = u - a.tile_unit[lo];
+        for (int st = 0; st < nst; ++st) {
+            mbar_init(&s_full[st], 32);
+            mbar_init(&s_empty[st], kComputeWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    Unit un;
+    un.t = s_info[0];
+    const int64_t chunk = s_info[1];
+    un.c = a.tile_cell[un.t];
+    un.q0 = a.tile_q0[un.t];
+    un.nq = a.tile_nq[un.t];
+    un.B = a.bound[un.c];
+    un.W = (un.B + 31) >> 5;
+    un.W4 = (un.W + 3) & ~int64_t(3);
+    un.ncell = a.nbr_cnt[un.c];
+    if (tid < un.ncell) {
+        const int32_t nb = a.nbr[(int64_t)un.c * kStencil + tid];
+        s_nstart[tid] = a.cell_start[nb];
+        s_vpre[tid + 1] = a.cell_start[nb + 1] - a.cell_start[nb];
+    }
+    __syncthreads();
+    if (tid == 0) {
+        s_vpre[0] = 0;
+        for (int i = 1; i <= un.ncell; ++i) s_vpre[i] += s_vpre[i - 1];
+    }
+    __syncthreads();
+    const int64_t ch = refine_chunk_of(a.d4);
+    un.vbeg = chunk * ch;
+    un.vend = min(un.B, un.vbeg + ch);
+    un.ntiles = (int)((un.vend - un.vbeg + TP - 1) / TP);
+    return un;
+}
+
+// The producer warp: streams the unit's chunk through the stage ring.  Each
+// lane copies the 16-byte chunks of the staged dimensions (C4 chunks) of rows
+// lane and lane + 32 of a tile (cp.async), then arrives on the stage's full
+// barrier twice: once asynchronously when its copies land, once now.  With
+// partly staged rows it also records each row's index (-1 past the chunk
+// end).
+template <int TP>
+__device__ __forceinline__ void produce(const RefineArgs &a, const Unit &un, float *P0, int32_t *s_row, int S, int C4,
+                                        int d4, bool partial_rows, int nst, uint64_t *s_full, uint64_t *s_empty,
+                                        const int32_t *s_nstart, const int32_t *s_vpre, int lane)
+{
+    for (int it = 0; it < un.ntiles; ++it) {
+        const int st = it % nst;
+        const uint32_t round = (uint32_t)(it / nst);
+        if (it >= nst && !refine_wait(&s_empty[st], (round - 1u) & 1u)) {
+            atomicExch(&a.flags[kFlagRefineTimeout], 1);
+            return;
+        }
+        float *P = P0 + st * TP * S;
+        const int64_t v0 = un.vbeg + (int64_t)it * TP;
+#pragma unroll
+        for (int h = 0; h < TP / 32; ++h) {
+            const int r = lane + 32 * h;
+            const int64_t v = v0 + r;
+            float4 *row = reinterpret_cast<float4 *>(P + r * S);
+            if (v < un.vend) {
+                int lo = 0, hi = un.ncell - 1;  // last slot with s_vpre[slot] <= v
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (s_vpre[mid] <= v) lo = mid; else hi = mid - 1;
+                }
+                const int32_t grow = s_nstart[lo] + (int32_t)(v - s_vpre[lo]);
+                const float *src = a.xs + (int64_t)grow * d4;
+                for (int cc = 0; cc < C4; ++cc) cp_async16(row + cc, src + 4 * cc);
+                if (partial_rows) s_row[st * TP + r] = grow;
+            } else {
+                // no candidate: -inf makes every distance to this row +inf
+                for (int cc = 0; cc < C4; ++cc) row[cc] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                if (partial_rows) s_row[st * TP + r] = -1;
+            }
+        }
+        cp_async_arrive_on(&s_full[st]);
+        mbar_arrive(&s_full[st]);
+    }
+}
+
 // One thread block refines one unit: a tile of up to TQ queries of one grid
 // cell against one chunk of up to kCH candidates of the cell's concatenated
 // stencil.  The producer warp streams the chunk through a ring of staged
@@ -516,88 +624,16 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
     uint16_t *s_sidx = reinterpret_cast<uint16_t *>(s_spart + kComputeWarps * kSurvMax);
     uint32_t *s_sword = reinterpret_cast<uint32_t *>(s_sidx + kComputeWarps * kSurvMax);
 
-    if (tid == 0) {
-        const int64_t u = a.unit0 + blockIdx.x;
-        int64_t lo = a.t0, hi = a.t1 - 1;  // last tile with tile_unit[t] <= u
-        while (lo < hi) {
-            const int64_t mid = (lo + hi + 1) >> 1;
-            if (a.tile_unit[mid] <= u) lo = mid; else hi = mid - 1;
-        }
-        s_info[0] = lo;
-        s_info[1] = u - a.tile_unit[lo];
-        for (int st = 0; st < nst; ++st) {
-            mbar_init(&s_full[st], 32);
-            mbar_init(&s_empty[st], kComputeWarps);
-        }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
-    const int64_t t = s_info[0];
-    const int64_t chunk = s_info[1];
-    const int32_t c = a.tile_cell[t];
-    const int32_t q0 = a.tile_q0[t];
-    const int nq = a.tile_nq[t];
-    const int64_t B = a.bound[c];
-    const int64_t W = (B + 31) >> 5;           // meaningful words of a mask row
-    const int64_t W4 = (W + 3) & ~int64_t(3);  // row stride (16-byte rows)
-    const int ncell = a.nbr_cnt[c];
-    if (tid < ncell) {
-        const int32_t nb = a.nbr[(int64_t)c * kStencil + tid];
-        s_nstart[tid] = a.cell_start[nb];
-        s_vpre[tid + 1] = a.cell_start[nb + 1] - a.cell_start[nb];
-    }
-    __syncthreads();
-    if (tid == 0) {
-        s_vpre[0] = 0;
-        for (int i = 1; i <= ncell; ++i) s_vpre[i] += s_vpre[i - 1];
-    }
-    __syncthreads();
-
-    const int64_t vbeg = chunk * kCH;
-    const int64_t vend = min(B, vbeg + (int64_t)kCH);
-    const int ntiles = (int)((vend - vbeg + kTP - 1) / kTP);
+    const Unit un = unit_begin<kTP>(a, nst, s_full, s_empty, s_nstart, s_vpre, s_info);
+    const int64_t t = un.t;
+    const int32_t q0 = un.q0;
+    const int nq = un.nq;
+    const int64_t W = un.W, W4 = un.W4;
+    const int64_t vbeg = un.vbeg, vend = un.vend;
+    const int ntiles = un.ntiles;
 
     if (warp == kComputeWarps) {
-        // ---- producer warp: stream the chunk through the stage ring ----
-        // Each lane copies the 16-byte chunks of the staged dimensions of
-        // rows lane and lane + 32 of a tile (cp.async), then arrives on the
-        // stage's full barrier twice: once asynchronously when its copies
-        // land, once now.  With partly staged rows it also records each
-        // row's index (-1 past the chunk end).
-        for (int it = 0; it < ntiles; ++it) {
-            const int st = it % nst;
-            const uint32_t round = (uint32_t)(it / nst);
-            if (it >= nst && !refine_wait(&s_empty[st], (round - 1u) & 1u)) {
-                atomicExch(&a.flags[kFlagRefineTimeout], 1);
-                return;
-            }
-            float *P = P0 + st * kTP * S;
-            const int64_t v0 = vbeg + (int64_t)it * kTP;
-#pragma unroll
-            for (int h = 0; h < kTP / 32; ++h) {
-                const int r = lane + 32 * h;
-                const int64_t v = v0 + r;
-                float4 *row = reinterpret_cast<float4 *>(P + r * S);
-                if (v < vend) {
-                    int lo = 0, hi = ncell - 1;  // last slot with s_vpre[slot] <= v
-                    while (lo < hi) {
-                        const int mid = (lo + hi + 1) >> 1;
-                        if (s_vpre[mid] <= v) lo = mid; else hi = mid - 1;
-                    }
-                    const int32_t grow = s_nstart[lo] + (int32_t)(v - s_vpre[lo]);
-                    const float *src = a.xs + (int64_t)grow * d4;
-                    for (int cc = 0; cc < C4; ++cc) cp_async16(row + cc, src + 4 * cc);
-                    if (partial_rows) s_row[st * kTP + r] = grow;
-                } else {
-                    // no candidate: -inf makes every distance to this row +inf
-                    for (int cc = 0; cc < C4; ++cc)
-                        row[cc] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-                    if (partial_rows) s_row[st * kTP + r] = -1;
-                }
-            }
-            cp_async_arrive_on(&s_full[st]);
-            mbar_arrive(&s_full[st]);
-        }
+        produce<kTP>(a, un, P0, s_row, S, C4, d4, partial_rows, nst, s_full, s_empty, s_nstart, s_vpre, lane);
         return;
     }
 
@@ -1018,7 +1054,7 @@ cudaError_t refine_profile(const RefineArgs &a, cudaStream_t s, int64_t *launche
     return a.d4 <= 64 ? launch_refine<8, 4, true>(a, s) : launch_refine<4, 4, true>(a, s);
 }
 
-int refine_chunk(int) { return kCH; }
+int refine_chunk(int d4) { return refine_chunk_of(d4); }
 
 cudaError_t compact(const CompactArgs &a, cudaStream_t s, int64_t *launches)
 {

@@ -106,9 +106,9 @@ __global__ void __launch_bounds__(128, 1) k_gram_tf32(const float *a, const floa
 // g = (K + 24) 2^-22, make the signs decisive:
 //     u < 0                   => dist(q, p) <  eps  (bit 1),
 //     u > 2 (alpha + beta)    => dist(q, p) >  eps  (bit 0),
-// and only pairs with 0 <= u <= 2 (alpha + beta) are rechecked exactly: the
-// float32 squared distance summed in dimension order, bit = sum <= eps^2,
-// the arithmetic of the CUDA-core refinement.
+// and only pairs with 0 <= u <= 2 (alpha + beta) are rechecked exactly with
+// the CUDA-core refinement's float32 arithmetic (refine_dist2), bit =
+// sum <= eps^2.
 constexpr int kTcRows = 128;                 // queries per tile (M) = candidates per tile (N)
 constexpr int kTcThreads = 9 * 32;
 constexpr int kTcXf0 = 4 * 32;               // first transform thread
@@ -161,23 +161,11 @@ __device__ __forceinline__ void split_tf32(float x, float &hi, float &lo)
     lo = to_tf32(x - hi);  // x - hi is exact in float32
 }
 
-// Exact recheck of one pair: float32 squared distance in dimension order.
+// Exact recheck of one pair: the CUDA-core refinement's float32 squared
+// distance (refine_dist2).
 __device__ __noinline__ bool tc_recheck(const float *q, const float *p, int d4, float eps2)
 {
-    float s = 0.0f;
-    for (int k = 0; k < d4; k += 4) {
-        const float4 a = *reinterpret_cast<const float4 *>(q + k);
-        const float4 b = *reinterpret_cast<const float4 *>(p + k);
-        float e = a.x - b.x;
-        s = k == 0 ? e * e : fmaf(e, e, s);
-        e = a.y - b.y;
-        s = fmaf(e, e, s);
-        e = a.z - b.z;
-        s = fmaf(e, e, s);
-        e = a.w - b.w;
-        s = fmaf(e, e, s);
-    }
-    return s <= eps2;
+    return refine_dist2(q, p, d4) <= eps2;
 }
 
 // Stage 128 rows into a K-major core-matrix operand with the 4 transform
