@@ -104,11 +104,16 @@ __host__ __device__ __forceinline__ constexpr int staged_dims(int d4)
 #endif
 constexpr int kSurvMax = 64;  // survivors a warp takes at a time (a multiple of 32)
 // 16-byte chunks of a candidate row a survivor loads from global memory at
-// once (its latency is paid once per chunk group)
+// once (its latency is paid once per chunk group).  Measured on GB300:
+// spectrum (d4 = 128) 397 / 374 / 490 ms and subspace (d4 = 64) 2.39 / 2.57 /
+// 5.03 s with 2 / 4 / 8 chunks (8 spills registers of the blocked loop).
 #ifndef HISS_SURV_AHEAD
 #define HISS_SURV_AHEAD 4
 #endif
-constexpr int kSurvAhead = HISS_SURV_AHEAD;
+#ifndef HISS_SURV_AHEAD64
+#define HISS_SURV_AHEAD64 2
+#endif
+__host__ __device__ __forceinline__ constexpr int surv_ahead(int d4) { return d4 <= 64 ? HISS_SURV_AHEAD64 : HISS_SURV_AHEAD; }
 // Dimension after which a warp may switch to survivor mode (a multiple of 4),
 // 0 for none.
 __host__ __device__ __forceinline__ constexpr int surv_dim(int mq, int d4)
@@ -336,7 +341,7 @@ __device__ __forceinline__ void live_scan(const f32x2 (&acc)[MQ / 2][MP], float 
 // bits of the pairs within eps^2 are gathered in sword[query row of the warp
 // tile] (bit = candidate column), ready for the caller after the closing
 // __syncwarp.
-template <int MQ, int MP>
+template <int MQ, int MP, int AHEAD>
 __device__ __forceinline__ void survivors(const f32x2 (&acc)[MQ / 2][MP], const float *Q2, const float *P,
                                           const float *xs, const int32_t *srow, int S2, int S, int k, int ds, int d4,
                                           float eps2, int first, int total, int lane, int wq, int wp, float *spart,
@@ -366,24 +371,23 @@ __device__ __forceinline__ void survivors(const f32x2 (&acc)[MQ / 2][MP], const 
             const int code = sidx[e];
             const int r = code >> 5, pc = code & 31;
             const int qt = wq * (4 * MQ) + r;  // query row of the tile
-            const float *qrow = Q2 + (4 * (qt >> 3) + (qt & 3)) * S2;
-            const bool hi = ((qt >> 2) & 1) != 0;  // second row of its pair row
+            // the query's values: every other float of its pair row, from the
+            // first or the second slot
+            const float *qv = Q2 + (4 * (qt >> 3) + (qt & 3)) * S2 + ((qt >> 2) & 1);
             const int prow_i = wp * (8 * MP) + pc;
             const float *prow = P + prow_i * S;
             float sum = spart[e];
             int kk = k;
             for (; kk < ds; kk += 4) {
-                const float4 qa = *reinterpret_cast<const float4 *>(qrow + 2 * kk);
-                const float4 qb = *reinterpret_cast<const float4 *>(qrow + 2 * kk + 4);
                 const float4 pv = *reinterpret_cast<const float4 *>(prow + kk);
                 float df;
-                df = __fsub_rn(hi ? qa.y : qa.x, pv.x);
+                df = __fsub_rn(qv[2 * kk], pv.x);
                 sum = __fmaf_rn(df, df, sum);
-                df = __fsub_rn(hi ? qa.w : qa.z, pv.y);
+                df = __fsub_rn(qv[2 * kk + 2], pv.y);
                 sum = __fmaf_rn(df, df, sum);
-                df = __fsub_rn(hi ? qb.y : qb.x, pv.z);
+                df = __fsub_rn(qv[2 * kk + 4], pv.z);
                 sum = __fmaf_rn(df, df, sum);
-                df = __fsub_rn(hi ? qb.w : qb.z, pv.w);
+                df = __fsub_rn(qv[2 * kk + 6], pv.w);
                 sum = __fmaf_rn(df, df, sum);
                 if (sum > eps2) break;
             }
@@ -392,25 +396,23 @@ __device__ __forceinline__ void survivors(const f32x2 (&acc)[MQ / 2][MP], const 
                 // (a live pair's candidate is a real row: padding rows are at
                 // +inf distance)
                 const float4 *pg = reinterpret_cast<const float4 *>(xs + (int64_t)srow[prow_i] * d4);
-                for (; kk < d4; kk += 4 * kSurvAhead) {
-                    float4 pv[kSurvAhead];
+                for (; kk < d4; kk += 4 * AHEAD) {
+                    float4 pv[AHEAD];
 #pragma unroll
-                    for (int u = 0; u < kSurvAhead; ++u)
+                    for (int u = 0; u < AHEAD; ++u)
                         if (kk + 4 * u < d4) pv[u] = __ldg(pg + (kk >> 2) + u);
 #pragma unroll
-                    for (int u = 0; u < kSurvAhead; ++u) {
+                    for (int u = 0; u < AHEAD; ++u) {
                         const int k4 = kk + 4 * u;
                         if (k4 < d4) {
-                            const float4 qa = *reinterpret_cast<const float4 *>(qrow + 2 * k4);
-                            const float4 qb = *reinterpret_cast<const float4 *>(qrow + 2 * k4 + 4);
                             float df;
-                            df = __fsub_rn(hi ? qa.y : qa.x, pv[u].x);
+                            df = __fsub_rn(qv[2 * k4], pv[u].x);
                             sum = __fmaf_rn(df, df, sum);
-                            df = __fsub_rn(hi ? qa.w : qa.z, pv[u].y);
+                            df = __fsub_rn(qv[2 * k4 + 2], pv[u].y);
                             sum = __fmaf_rn(df, df, sum);
-                            df = __fsub_rn(hi ? qb.y : qb.x, pv[u].z);
+                            df = __fsub_rn(qv[2 * k4 + 4], pv[u].z);
                             sum = __fmaf_rn(df, df, sum);
-                            df = __fsub_rn(hi ? qb.w : qb.z, pv[u].w);
+                            df = __fsub_rn(qv[2 * k4 + 6], pv[u].w);
                             sum = __fmaf_rn(df, df, sum);
                         }
                     }
@@ -823,7 +825,7 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
                 }
             }
             if (uses_survivors<false>(MQ, d4) && surv)
-                survivors<MQ, MP>(acc, Q2, P, a.xs, s_row + st * kTP, S2, S, sk, ds, d4, eps2, sfirst, stotal, lane,
+                survivors<MQ, MP, surv_ahead(D4 > 0 ? D4 : 64)>(acc, Q2, P, a.xs, s_row + st * kTP, S2, S, sk, ds, d4, eps2, sfirst, stotal, lane,
                                   wq, wp, s_spart + warp * kSurvMax, s_sidx + warp * kSurvMax, s_sword + warp * 32);
             // one bit per pair.  The warp's 32 candidate columns (pbase + 8 j)
             // form one mask word per query row: bit lp + 8 j.  A ballot per
