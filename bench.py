@@ -306,7 +306,7 @@ def cpu_baseline(x, eps, rows_req):
     dt = time.perf_counter() - t0
     return {"value": int(row_ptr[-1]) / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
             "cpu_model": cpu_model(), "omp_proc_bind": os.environ.get("OMP_PROC_BIND"),
-            "sample": ("the full join" if full else "%d random query rows") % q.size
+            "sample": ("the full join (%d query rows)" if full else "%d random query rows") % q.size
                       + " x all %d points, fp64 brute force, %.1f s" % (n, dt),
             "candidate_evals_per_s": q.size * n / dt,
             "full_join_s": dt * n / q.size, "full_join_s_kind": "measured" if full else "extrapolated"}
