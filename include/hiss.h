@@ -287,13 +287,13 @@ int hiss_set_option(hiss_ctx *ctx, int option, int64_t value);
  * hiss_join's refinement kernel actually evaluates, whose warps skip a
  * block of pairs when the boxes of its queries and candidates over the three
  * index dimensions are farther apart than eps, and otherwise abandon it only
- * when all of its pairs exceed eps^2 (checked after every 2
- * dimensions up to d4 = 64, from the 10th at d4 = 16 and the 6th at
- * d4 = 32 on, and after every 4 above d4 = 64); from d4 = 64 on, a warp left
- * with at most 64 pairs within eps^2 after 16 (d4 = 64) or 48 (d4 > 64)
- * dimensions finishes those pairs alone, each stopping when it exceeds
- * eps^2.  out is a host int64[2].  Costs about one
- * join's refinement with no early termination. */
+ * when all of its pairs exceed eps^2 (checked after every 2 dimensions up to
+ * d4 = 64, from the 10th at d4 = 16 and the 6th at d4 = 32 on, and after
+ * every 4 above d4 = 64); from d4 = 64 on, a warp left with at most 64 pairs
+ * within eps^2 after 16 dimensions, or with any when the dimensions staged in
+ * shared memory run out (16 at d4 = 64, 32 above), finishes those pairs
+ * alone, each stopping when it exceeds eps^2.  out is a host int64[2].
+ * Costs about one join's refinement with no early termination. */
 int hiss_work_profile(hiss_ctx *ctx, float eps, int64_t *out);
 
 /* ---- building blocks exposed for testing ---------------------------------
