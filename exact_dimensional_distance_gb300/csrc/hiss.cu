@@ -73,6 +73,7 @@ struct hiss_ctx {
     // pinned staging, a copy stream and its events (created on first use)
     DBuf row_ptr2, cols2, query_ids2, query_rows2;
     DBuf row_ptr_sub;  // row offsets of a batch delivered in parts
+    DBuf unit_tile, unit_chunk;  // order in which a batch's refinement blocks take its units
     void *h_pinned2 = nullptr;
     size_t h_cap2 = 0;
     cudaStream_t copy_stream = nullptr;
@@ -516,6 +517,18 @@ int ensure_copy_stream(hiss_ctx *ctx)
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
+// Above 32 dimensions the refinement blocks take a batch's units chunk by
+// chunk within each cell (unit_order) rather than tile by tile, so that
+// blocks running together read the same candidate rows (which the
+// survivors re-read from global memory).  Measured on GB300: subspace (d4 =
+// 64) 2.44 -> 2.35 s, spectrum (d4 = 128) 385 -> 366 ms; gmm (d4 = 32) no
+// change; exp (d4 = 16) 12.91 -> 13.14 s, so builds up to 32 dimensions keep
+// the tile order.
+#ifndef HISS_UNIT_ORDER_MIN_D4
+#define HISS_UNIT_ORDER_MIN_D4 33
+#endif
+bool chunk_major(int d4) { return d4 >= HISS_UNIT_ORDER_MIN_D4; }
+
 // Plan the batches over the current tiles and run them: refinement,
 // compaction, delivery and the callback, batch by batch.
 // tlo, thi: the query tiles (processing order) to run; thi < 0 means all.
@@ -564,12 +577,17 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
     CK(cudaMemcpyAsync(info.data(), ctx->binfo.p, 32 * (size_t)(nb + 1), cudaMemcpyDeviceToHost, s));
     ST(sync(ctx));
 
-    int64_t max_words = 0, max_nq = 0, max_cost = 0;
+    int64_t max_words = 0, max_nq = 0, max_cost = 0, max_units = 0;
     for (int64_t b = 0; b < nb; ++b) {
         const int64_t dw = info[4 * (b + 1)] - info[4 * b], dq = info[4 * (b + 1) + 2] - info[4 * b + 2];
         max_words = std::max(max_words, dw);
         max_nq = std::max(max_nq, dq);
         max_cost = std::max(max_cost, dw + (dw >> 5) + 2 + per_query_words * dq);
+        max_units = std::max(max_units, info[4 * (b + 1) + 1] - info[4 * b + 1]);
+    }
+    if (!tc && chunk_major(ctx->d4)) {
+        ST(ensure(ctx, ctx->unit_tile, 4 * (size_t)max_units));
+        ST(ensure(ctx, ctx->unit_chunk, 4 * (size_t)max_units));
     }
     // CSR columns per delivery (per slot with the overlapped delivery)
     const int64_t cols_cap = std::max<int64_t>(1, (budget_words - max_cost) / (ov ? 2 : 1));
@@ -648,6 +666,12 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
         ra.eps2 = eps * eps;
         ra.prof = nullptr;
         ra.flags = as<int>(ctx->flags);
+        if (!tc && chunk_major(ctx->d4)) {
+            CK(unit_order(ra, qs.qcell_start, refine_tq(ctx->d4), as<int32_t>(ctx->unit_tile),
+                          as<int32_t>(ctx->unit_chunk), s, &ctx->launches));
+            ra.unit_tile = as<int32_t>(ctx->unit_tile);
+            ra.unit_chunk = as<int32_t>(ctx->unit_chunk);
+        }
         CK(cudaEventRecord(ctx->ev[4], s));
         if (tc) CK(refine_tc(ra, eps, s, &ctx->launches));
         else CK(refine(ra, s, &ctx->launches));
@@ -1214,7 +1238,7 @@ void hiss_destroy(hiss_ctx *ctx)
                    &ctx->q_cell_of_row, &ctx->q_cell_start, &ctx->q_cell_key, &ctx->q_nbr, &ctx->q_nbr_cnt,
                    &ctx->q_bound, &ctx->q_work_key, &ctx->q_cell_idx, &ctx->q_work, &ctx->k_keys,
                    &ctx->k_vals, &ctx->k_keys_alt, &ctx->k_vals_alt, &ctx->k_sort_tmp, &ctx->k_d2, &ctx->k_prow,
-                   &ctx->k_done, &ctx->k_active, &ctx->row_ptr2, &ctx->cols2, &ctx->row_ptr_sub,
+                   &ctx->k_done, &ctx->k_active, &ctx->row_ptr2, &ctx->cols2, &ctx->row_ptr_sub, &ctx->unit_tile, &ctx->unit_chunk,
                    &ctx->query_ids2, &ctx->query_rows2};
     if (ctx->copy_stream) cudaStreamSynchronize(ctx->copy_stream);
     for (DBuf *b : all) release(ctx, *b);

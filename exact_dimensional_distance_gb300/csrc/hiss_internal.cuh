@@ -109,6 +109,8 @@ struct RefineArgs {
     const int64_t *tile_qoff;   // [T+1] first query (absolute, processing order)
     int64_t t0, t1;             // batch: tiles [t0, t1)
     int64_t unit0, nunits;      // units of the batch
+    const int32_t *unit_tile;   // [nunits] tile of block u (NULL: found by search, units in tile order)
+    const int32_t *unit_chunk;  // [nunits] candidate chunk of block u
     int64_t word0, q0;          // batch origin in words and queries
     uint32_t *mask;             // batch mask: only nonzero words are written
     uint32_t *occ;              // occupancy: bit (w & 31) of occ[w >> 5] set when mask word w is nonzero (zeroed per batch)
@@ -143,6 +145,14 @@ __device__ __forceinline__ float refine_dist2(const float *q, const float *p, in
     return s;
 }
 cudaError_t refine(const RefineArgs &a, cudaStream_t s, int64_t *launches);
+// The order in which a batch's blocks take its units: within each cell's run
+// of tiles in the batch, chunk by chunk (every query tile of the cell on
+// candidate chunk 0, then chunk 1, ...), so that blocks running at the same
+// time read the same candidate rows.  Fills unit_tile / unit_chunk (device
+// arrays of a.nunits entries) from the batch's tiles; qcell_start: the query
+// side's cell ranges (the data's own for the self-join).
+cudaError_t unit_order(const RefineArgs &a, const int32_t *qcell_start, int tq, int32_t *unit_tile,
+                       int32_t *unit_chunk, cudaStream_t s, int64_t *launches);
 cudaError_t refine_profile(const RefineArgs &a, cudaStream_t s, int64_t *launches);
 
 struct CompactArgs {

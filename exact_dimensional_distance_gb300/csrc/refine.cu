@@ -493,14 +493,19 @@ __device__ __forceinline__ Unit unit_begin(const RefineArgs &a, int nst, uint64_
 {
     const int tid = threadIdx.x;
     if (tid == 0) {
-        const int64_t u = a.unit0 + blockIdx.x;
-        int64_t lo = a.t0, hi = a.t1 - 1;  // last tile with tile_unit[t] <= u
-        while (lo < hi) {
-            const int64_t mid = (lo + hi + 1) >> 1;
-            if (a.tile_unit[mid] <= u) lo = mid; else hi = mid - 1;
+        if (a.unit_tile) {
+            s_info[0] = a.unit_tile[blockIdx.x];
+            s_info[1] = a.unit_chunk[blockIdx.x];
+        } else {
+            const int64_t u = a.unit0 + blockIdx.x;
+            int64_t lo = a.t0, hi = a.t1 - 1;  // last tile with tile_unit[t] <= u
+            while (lo < hi) {
+                const int64_t mid = (lo + hi + 1) >> 1;
+                if (a.tile_unit[mid] <= u) lo = mid; else hi = mid - 1;
+            }
+            s_info[0] = lo;
+            s_info[1] = u - a.tile_unit[lo];
         }
-        s_info[0] = lo;
-        s_info[1] = u - a.tile_unit[lo];
         for (int st = 0; st < nst; ++st) {
             mbar_init(&s_full[st], 32);
             mbar_init(&s_empty[st], kComputeWarps);
@@ -1026,7 +1031,41 @@ __global__ void k_word_positions(const uint32_t *words, int64_t nbits, const int
     }
 }
 
+// One thread per tile of the batch: its units go to positions chunk x (tiles
+// of its cell in the batch) + (its rank among them), counted from the unit
+// of the first of those tiles.  A cell's tiles are consecutive in
+// processing order and share one chunk count.
+__global__ void k_unit_order(const RefineArgs a, const int32_t *qcell_start, int tq, int32_t *unit_tile,
+                             int32_t *unit_chunk)
+{
+    const int64_t t = a.t0 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= a.t1) return;
+    const int32_t c = a.tile_cell[t];
+    const int32_t s0 = qcell_start[c], sz = qcell_start[c + 1] - s0;
+    const int64_t first = t - (a.tile_q0[t] - s0) / tq;     // the cell's first tile
+    const int64_t ta = max(first, a.t0);
+    const int64_t tb = min(first + (sz + tq - 1) / tq, a.t1);
+    const int64_t nt = tb - ta;
+    const int64_t base = a.tile_unit[ta] - a.unit0;
+    const int64_t k_units = a.tile_unit[t + 1] - a.tile_unit[t];
+    for (int64_t k = 0; k < k_units; ++k) {
+        const int64_t u = base + k * nt + (t - ta);
+        unit_tile[u] = (int32_t)t;
+        unit_chunk[u] = (int32_t)k;
+    }
+}
+
 }  // namespace
+
+cudaError_t unit_order(const RefineArgs &a, const int32_t *qcell_start, int tq, int32_t *unit_tile,
+                       int32_t *unit_chunk, cudaStream_t s, int64_t *launches)
+{
+    const int64_t nt = a.t1 - a.t0;
+    if (nt <= 0) return cudaSuccess;
+    k_unit_order<<<(unsigned)((nt + 255) / 256), 256, 0, s>>>(a, qcell_start, tq, unit_tile, unit_chunk);
+    ++*launches;
+    return cudaGetLastError();
+}
 
 int refine_tq(int d4) { return d4 <= 64 ? Geo<8, 4>::TQ : Geo<4, 4>::TQ; }
 

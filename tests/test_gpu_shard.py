@@ -20,11 +20,14 @@ def _edd():
     return edd
 
 
-@pytest.mark.parametrize("nranks", [1, 2, 3, 7])
-def test_shards_partition_the_join(nranks):
+@pytest.mark.parametrize("cfg,n,nranks,batch_bytes", [(1, None, 1, 0), (1, None, 2, 0), (1, None, 3, 0),
+                                                     (1, None, 7, 0), (4, 6000, 3, 1 << 20), (3, 8000, 2, 1 << 20)])
+def test_shards_partition_the_join(cfg, n, nranks, batch_bytes):
+    # cfg 3 and 4 (d = 64, 128) run the chunk-by-chunk unit order, whose cell
+    # runs are cut by shard and batch boundaries here
     edd = _edd()
-    x = datagen.generate(1)
-    eps = golden_eps(1)
+    x = datagen.generate(cfg, n=n)
+    eps = golden_eps(cfg) if n is None else float(np.float32(golden_eps(cfg) * 1.5))
     j = edd.Join()
     j.build(torch.from_numpy(x).cuda())
     full = j.join_sets(eps)
@@ -32,7 +35,7 @@ def test_shards_partition_the_join(nranks):
     seen = {}
     units = []
     for r in range(nranks):
-        part = j.join_shard_sets(eps, r, nranks)
+        part = j.join_shard_sets(eps, r, nranks, batch_bytes)
         units.append(j.stats()["refine_units"])
         for q, cols in part.items():
             assert q not in seen, "query %d in two shards" % q
