@@ -64,20 +64,32 @@ def load_eps(cfg):
         return json.load(f)[str(cfg)]["eps"]
 
 
+def code_sha(path):
+    """sha256 prefix of a source file's code: comments (from // to the end of
+    a line) and blank lines left out, so that comment edits keep it."""
+    import hashlib
+    import re
+    lines = []
+    for line in open(path, encoding="utf-8"):
+        line = re.sub(r"//.*$", "", line).rstrip()
+        if line:
+            lines.append(line)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
+
+
 def refine_traffic_per_unit(cfg):
     """DRAM bytes per refinement unit of workload cfg from the committed ncu
-    figures (profiles/k_refine_traffic.json), or None when refine.cu has
-    changed since those counters were taken."""
-    import hashlib
+    figures (profiles/k_refine_traffic.json), or None when the code of
+    refine.cu has changed since those counters were taken."""
     src = os.path.join(ROOT, "exact_dimensional_distance_gb300", "csrc", "refine.cu")
     path = os.path.join(ROOT, "profiles", "k_refine_traffic.json")
     try:
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        sha = code_sha(src)
         with open(path) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    if rec.get("refine_cu_sha256_16") != sha:
+    if rec.get("refine_cu_code_sha256_16") != sha:
         return None
     ent = rec.get("workloads", {}).get(str(cfg))
     return None if ent is None else float(ent["dram_bytes_per_unit"])

@@ -6,18 +6,21 @@
 // it, concatenated in stencil order).  The query tile stays in shared memory
 // (two query rows interleaved per pair row).  A producer warp streams the
 // candidates through a ring of shared-memory stages, gathering each candidate
-// row from its stencil cell with cp.async, completion tracked by mbarriers.
-// Each compute thread owns an 8 x 4 block of (query, candidate) squared
-// distances (4 x 4 above 64 dimensions), held as packed float32 pairs, and
-// adds two dimensions per step with f32x2 subtract / multiply-add
-// instructions (one instruction per pair and dimension instead of two).
-// Dimensions are in variance order, so after every 2 dimensions (8 x 4
-// blocks) or 4 (4 x 4 blocks) a warp checks whether all of its partial sums
-// already exceed eps^2 and, if so, leaves the tile (early termination,
-// Section IV-A); at 64 dimensions and more, a warp left with few pairs
-// within eps^2 finishes them one pair per lane.  The result is one
-// bit per pair, sum <= eps^2, written to the query's mask row; the popcount
-// of each word is accumulated into the query's neighbour count.
+// row (its first 16 or 32 dimensions above 32) from its stencil cell with
+// cp.async, completion tracked by mbarriers.  Each compute thread owns an
+// 8 x 4 block of (query, candidate) squared distances (4 x 4 above 64
+// dimensions), held as packed float32 pairs, and adds two dimensions per
+// step with f32x2 subtract / multiply-add instructions (one instruction per
+// pair and dimension instead of two).  Before any arithmetic a warp skips a
+// staged tile whose box over the three index dimensions is farther than eps
+// from its queries' box.  Dimensions are in variance order, so after every
+// 2 dimensions (8 x 4 blocks) or 4 (4 x 4 blocks) a warp checks whether all
+// of its partial sums already exceed eps^2 and, if so, leaves the tile
+// (early termination, Section IV-A); at 64 dimensions and more, a warp left
+// with few pairs within eps^2, or with any when the staged dimensions run
+// out, finishes them one pair per lane.  The result is one bit per pair,
+// sum <= eps^2, written to the query's mask row; the popcount of each word
+// is accumulated into the query's neighbour count.
 #include "hiss_internal.cuh"
 #include "ptx.cuh"
 

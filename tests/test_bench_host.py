@@ -39,3 +39,13 @@ def test_reference_arm_prints_one_line(capsys, monkeypatch):
     line = json.loads(capsys.readouterr().out.strip())
     assert line["impl"] == "reference" and line["unit"] == bench.UNIT and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_code_sha_ignores_comments_not_code(tmp_path):
+    a = tmp_path / "a.cu"
+    a.write_text("int f() {\n    return 1;  // one\n}\n")
+    b = tmp_path / "b.cu"
+    b.write_text("// a comment\nint f() {\n\n    return 1;\n}\n")
+    c = tmp_path / "c.cu"
+    c.write_text("int f() {\n    return 2;\n}\n")
+    assert bench.code_sha(str(a)) == bench.code_sha(str(b)) != bench.code_sha(str(c))
