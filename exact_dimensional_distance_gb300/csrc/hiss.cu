@@ -50,6 +50,7 @@ struct hiss_ctx {
     GridParams gp{};
     int64_t C = 0, cell_pairs = 0, candidates = 0;
     DBuf keys, vals, keys_alt, vals_alt, sort_tmp, xs, ids, flag, flag_scan, cell_start, cell_key, cell_of_row;
+    DBuf gbox;  // boxes of xs's 32-row groups over the index dimensions
     DBuf nbr, nbr_cnt, bound, work_key, cell_idx, work, scan_tmp, sums2;
     uint64_t *sorted_keys = nullptr;
     uint32_t *sorted_vals = nullptr;
@@ -311,6 +312,8 @@ int ensure_grid(hiss_ctx *ctx, float eps)
     ctx->sorted_vals = in_alt ? as<uint32_t>(ctx->vals_alt) : as<uint32_t>(ctx->vals);
     CK(gather_rows(as<float>(ctx->xv), ctx->sorted_vals, n, d4, as<float>(ctx->xs), as<int32_t>(ctx->ids), s,
                    &ctx->launches));
+    ST(ensure(ctx, ctx->gbox, 32 * (size_t)((n + 31) / 32) + 32));
+    CK(group_boxes(as<float>(ctx->xs), n, d4, as<float4>(ctx->gbox), s, &ctx->launches));
     const int shift = 3 * gp.sub_bits;
     CK(cell_flags(ctx->sorted_keys, n, shift, as<int32_t>(ctx->flag), s, &ctx->launches));
     CK(scan_i32(as<int32_t>(ctx->flag), as<int32_t>(ctx->flag_scan), n, as<int64_t>(ctx->scan_tmp), s,
@@ -665,6 +668,7 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
         ra.d = ctx->d;
         ra.eps2 = eps * eps;
         ra.prof = nullptr;
+        ra.gbox = as<float4>(ctx->gbox);
         ra.flags = as<int>(ctx->flags);
         if (!tc && chunk_major(ctx->d4)) {
             CK(unit_order(ra, qs.qcell_start, refine_tq(ctx->d4), as<int32_t>(ctx->unit_tile),
@@ -1227,7 +1231,7 @@ void hiss_destroy(hiss_ctx *ctx)
     cudaSetDevice(ctx->device);
     cudaStreamSynchronize(ctx->stream);
     DBuf *all[] = {&ctx->x_stage, &ctx->xv, &ctx->perm_d, &ctx->stats_partial, &ctx->stats_out, &ctx->flags,
-                   &ctx->keys, &ctx->vals, &ctx->keys_alt, &ctx->vals_alt, &ctx->sort_tmp, &ctx->xs, &ctx->ids,
+                   &ctx->keys, &ctx->vals, &ctx->keys_alt, &ctx->vals_alt, &ctx->sort_tmp, &ctx->xs, &ctx->gbox, &ctx->ids,
                    &ctx->flag, &ctx->flag_scan, &ctx->cell_start, &ctx->cell_key, &ctx->cell_of_row, &ctx->nbr,
                    &ctx->nbr_cnt, &ctx->bound, &ctx->work_key, &ctx->cell_idx, &ctx->work, &ctx->scan_tmp,
                    &ctx->sums2, &ctx->lpt_keys, &ctx->lpt_order, &ctx->ntiles, &ctx->tile_off, &ctx->tile_cell,

@@ -61,6 +61,9 @@ cudaError_t cell_keys(const float *xv, int64_t n, int d4, GridParams gp, uint64_
                       cudaStream_t s, int64_t *launches);
 cudaError_t gather_rows(const float *xv, const uint32_t *order, int64_t n, int d4, float *xs, int32_t *ids,
                         cudaStream_t s, int64_t *launches);
+// Per aligned 32-row group of xs: box over the first three dimensions,
+// gbox[2 g] = minima, gbox[2 g + 1] = maxima ((n + 31) / 32 groups).
+cudaError_t group_boxes(const float *xs, int64_t n, int d4, float4 *gbox, cudaStream_t s, int64_t *launches);
 cudaError_t cell_flags(const uint64_t *keys, int64_t n, int shift, int32_t *flag, cudaStream_t s, int64_t *launches);
 cudaError_t cell_starts(const uint64_t *keys, const int32_t *flag_scan, int64_t n, int shift, int32_t *cell_start,
                         uint64_t *cell_key, int32_t *cell_of_row, cudaStream_t s, int64_t *launches);
@@ -119,6 +122,7 @@ struct RefineArgs {
     int d;                      // true dimension (profile mode caps the last step at d)
     float eps2;
     int64_t *prof;              // profile mode: [2] counters (sum of per-pair exit dims, executed dims)
+    const float4 *gbox;         // boxes of xs's 32-row groups (see group_boxes); NULL: every staged tile is streamed
     int *flags;                 // device int[kNumFlags]; kFlagRefineTimeout set if a stage wait gave up
 };
 int refine_tq(int d4);

@@ -173,6 +173,37 @@ __global__ void k_gather_rows(const float4 *__restrict__ xv, const uint32_t *__r
     if (c == 0) ids[r] = (int32_t)src;
 }
 
+// Box of each aligned group of 32 index rows over the first three dimensions
+// (the grid's index dimensions; zero padding where d < 3): gbox[2 g] = the
+// minima, gbox[2 g + 1] = the maxima (fourth component 0).  One warp per group.
+__global__ void k_group_boxes(const float *__restrict__ xs, int64_t n, int d4, float4 *__restrict__ gbox)
+{
+    const int64_t g = ((int64_t)blockIdx.x * kT + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (g >= (n + 31) >> 5) return;  // whole warps leave together
+    const int64_t r = g * 32 + lane;
+    float lo0 = INFINITY, lo1 = INFINITY, lo2 = INFINITY, hi0 = -INFINITY, hi1 = -INFINITY, hi2 = -INFINITY;
+    if (r < n) {
+        const float4 f = *reinterpret_cast<const float4 *>(xs + r * d4);
+        lo0 = hi0 = f.x;
+        lo1 = hi1 = f.y;
+        lo2 = hi2 = f.z;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        lo0 = fminf(lo0, __shfl_xor_sync(0xffffffffu, lo0, o));
+        lo1 = fminf(lo1, __shfl_xor_sync(0xffffffffu, lo1, o));
+        lo2 = fminf(lo2, __shfl_xor_sync(0xffffffffu, lo2, o));
+        hi0 = fmaxf(hi0, __shfl_xor_sync(0xffffffffu, hi0, o));
+        hi1 = fmaxf(hi1, __shfl_xor_sync(0xffffffffu, hi1, o));
+        hi2 = fmaxf(hi2, __shfl_xor_sync(0xffffffffu, hi2, o));
+    }
+    if (lane == 0) {
+        gbox[2 * g] = make_float4(lo0, lo1, lo2, 0.f);
+        gbox[2 * g + 1] = make_float4(hi0, hi1, hi2, 0.f);
+    }
+}
+
 __global__ void k_cell_flags(const uint64_t *__restrict__ keys, int64_t n, int shift, int32_t *__restrict__ flag)
 {
     const int64_t r = (int64_t)blockIdx.x * kT + threadIdx.x;
@@ -432,6 +463,14 @@ cudaError_t gather_rows(const float *xv, const uint32_t *order, int64_t n, int d
     const int c4 = d4 / 4;
     k_gather_rows<<<blocks_for(n * c4), kT, 0, s>>>(reinterpret_cast<const float4 *>(xv), order, n, c4,
                                                    reinterpret_cast<float4 *>(xs), ids);
+    ++*launches;
+    return cudaGetLastError();
+}
+
+cudaError_t group_boxes(const float *xs, int64_t n, int d4, float4 *gbox, cudaStream_t s, int64_t *launches)
+{
+    if (n <= 0) return cudaSuccess;
+    k_group_boxes<<<blocks_for(((n + 31) >> 5) * 32), kT, 0, s>>>(xs, n, d4, gbox);
     ++*launches;
     return cudaGetLastError();
 }

@@ -11,9 +11,12 @@
 // 8 x 4 block of (query, candidate) squared distances (4 x 4 above 64
 // dimensions), held as packed float32 pairs, and adds two dimensions per
 // step with f32x2 subtract / multiply-add instructions (one instruction per
-// pair and dimension instead of two).  Before any arithmetic a warp skips a
-// staged tile whose box over the three index dimensions is farther than eps
-// from its queries' box.  Dimensions are in variance order, so after every
+// pair and dimension instead of two).  A block first drops the candidate
+// tiles whose rows' 32-row group boxes (over the three index dimensions,
+// built with the index) are all farther than eps from its query tile's box:
+// they are neither streamed nor refined.  Before any arithmetic a warp also
+// skips a staged tile whose exact box is farther than eps from its queries'
+// box.  Dimensions are in variance order, so after every
 // 2 dimensions (8 x 4 blocks) or 4 (4 x 4 blocks) a warp checks whether all
 // of its partial sums already exceed eps^2 and, if so, leaves the tile
 // (early termination, Section IV-A); at 64 dimensions and more, a warp left
@@ -431,11 +434,15 @@ __device__ __forceinline__ void survivors(const f32x2 (&acc)[MQ / 2][MP], const 
 // Where a warp checks for early termination (k = dimensions summed so far):
 // with 8 x 4 blocks (d4 <= 64) after every 2 dimensions from the first check
 // on, with 4 x 4 blocks after every 4 (there the pairs leave later, and the
-// shorter steps need two per loop iteration to overlap their loads).  Where
-// the box test runs, it has already removed most of the tiles that an early
-// check would end, so the first check comes later: after 6 dimensions at
-// d4 = 32 and 10 at d4 = 16 (gmm refinement 35.2 ms with the first check
-// after 2, 34.4 after 6; exp 15.3 s after 2, 14.7 s after 10).
+// shorter steps need two per loop iteration to overlap their loads).  The box
+// test has already removed most of the tiles that an early check would end,
+// so the first check comes later: after 10 dimensions at d4 = 16, 6 at
+// d4 = 32, 8 at d4 = 64 (and at most half the dimensions elsewhere), 4 with
+// 4 x 4 blocks.  Measured on GB300 (refinement): exp (d = 16) 15.3 s with the
+// first check after 2, 14.7 s after 10; gmm (d = 32) 35.2 ms after 2, 34.4
+// after 6; subspace (d = 64) 2.35 / 2.32 / 2.30 / 2.29 / 2.32 / 2.39 s after
+// 2 / 4 / 6 / 8 / 10 / 12; spectrum (d = 128, 4 x 4 blocks) 366 / 366 /
+// 367 / 370 ms after 4 / 8 / 12 / 16.
 #ifndef HISS_FIRST_CHECK16
 #define HISS_FIRST_CHECK16 10
 #endif
@@ -443,16 +450,20 @@ __device__ __forceinline__ void survivors(const f32x2 (&acc)[MQ / 2][MP], const 
 #define HISS_FIRST_CHECK32 6
 #endif
 #ifndef HISS_FIRST_CHECK64
-#define HISS_FIRST_CHECK64 2
+#define HISS_FIRST_CHECK64 8
+#endif
+#ifndef HISS_FIRST_CHECK4
+#define HISS_FIRST_CHECK4 4
 #endif
 __host__ __device__ __forceinline__ constexpr int first_check(int d4)
 {
-    return d4 == 16 ? HISS_FIRST_CHECK16 : (d4 == 32 ? HISS_FIRST_CHECK32 : HISS_FIRST_CHECK64);
+    return d4 == 16 ? HISS_FIRST_CHECK16
+                    : (d4 == 32 ? HISS_FIRST_CHECK32 : (d4 / 2 < HISS_FIRST_CHECK64 ? d4 / 2 : HISS_FIRST_CHECK64));
 }
 template <int MQ>
 __device__ __forceinline__ bool exit_check_at(int k, int d4)
 {
-    return MQ == 8 ? k >= first_check(d4) : (k & 3) == 0;
+    return MQ == 8 ? k >= first_check(d4) : ((k & 3) == 0 && k >= HISS_FIRST_CHECK4);
 }
 
 
@@ -544,6 +555,111 @@ __device__ __forceinline__ Unit unit_begin(const RefineArgs &a, int nst, uint64_
     return un;
 }
 
+// Boxes of the query tile over the three index dimensions, and the staged
+// tiles of the unit worth streaming.
+//
+// s_qbox[8 g ...] = (lo0, lo1, lo2, hi0, hi1, hi2) of query rows g QG ...
+// g QG + QG - 1 (QG = 4 MQ, the rows of the compute warps with wq = g; no
+// row: +inf / -inf), for the compute warps' box test.
+//
+// Return value nkeep and s_list[0 .. nkeep): the staged tiles, in increasing
+// order, that are not provably farther than eps from every query of the tile
+// (tile it = candidate positions vbeg + it TP ...).  The test is the compute
+// warps' box test (below) on larger boxes: the query tile's box against the
+// union of the boxes of the 32-row groups of xs that hold the tile's
+// candidates.  Both contain the exact boxes, so the rounded gap bound is at
+// most that of any warp tile of the stage, and a skipped tile is one every
+// warp would have skipped.  Threads tid < ntiles each test one tile (a unit
+// has at most 128).  Without group boxes (and in the work-profile build)
+// every tile is kept.  All threads of the block call it.
+#ifndef HISS_STAGE_SKIP
+#define HISS_STAGE_SKIP 1
+#endif
+template <int TP, int TQ, int QG, bool PROF>
+__device__ __forceinline__ int stage_keep(const RefineArgs &a, const Unit &un, const int32_t *s_nstart,
+                                          const int32_t *s_vpre, float *s_qbox, uint32_t *s_keep, uint8_t *s_list)
+{
+    static_assert(kCH / TP <= 128 && TQ / 32 <= kComputeWarps && (QG == 16 || QG == 32), "keep mask geometry");
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (warp < TQ / 32) {
+        const int r = warp * 32 + lane;
+        float lo0 = INFINITY, lo1 = INFINITY, lo2 = INFINITY, hi0 = -INFINITY, hi1 = -INFINITY, hi2 = -INFINITY;
+        if (r < un.nq) {
+            const float4 f = *reinterpret_cast<const float4 *>(a.xq + (int64_t)(un.q0 + r) * a.d4);
+            lo0 = hi0 = f.x;
+            lo1 = hi1 = f.y;
+            lo2 = hi2 = f.z;
+        }
+#pragma unroll
+        for (int o = QG / 2; o > 0; o >>= 1) {
+            lo0 = fminf(lo0, __shfl_xor_sync(0xffffffffu, lo0, o));
+            lo1 = fminf(lo1, __shfl_xor_sync(0xffffffffu, lo1, o));
+            lo2 = fminf(lo2, __shfl_xor_sync(0xffffffffu, lo2, o));
+            hi0 = fmaxf(hi0, __shfl_xor_sync(0xffffffffu, hi0, o));
+            hi1 = fmaxf(hi1, __shfl_xor_sync(0xffffffffu, hi1, o));
+            hi2 = fmaxf(hi2, __shfl_xor_sync(0xffffffffu, hi2, o));
+        }
+        if ((lane & (QG - 1)) == 0) {
+            float *b = s_qbox + 8 * (r / QG);
+            b[0] = lo0, b[1] = lo1, b[2] = lo2, b[3] = hi0, b[4] = hi1, b[5] = hi2, b[6] = 0.f, b[7] = 0.f;
+        }
+    }
+    if (PROF || !HISS_STAGE_SKIP || a.gbox == nullptr) {
+        if (tid < un.ntiles) s_list[tid] = (uint8_t)tid;
+        __syncthreads();
+        return un.ntiles;
+    }
+    __syncthreads();
+    bool keep = false;
+    if (tid < un.ntiles) {
+        float qlo0 = s_qbox[0], qlo1 = s_qbox[1], qlo2 = s_qbox[2], qhi0 = s_qbox[3], qhi1 = s_qbox[4],
+              qhi2 = s_qbox[5];
+#pragma unroll
+        for (int w = 1; w < TQ / QG; ++w) {
+            const float *b = s_qbox + 8 * w;
+            qlo0 = fminf(qlo0, b[0]), qlo1 = fminf(qlo1, b[1]), qlo2 = fminf(qlo2, b[2]);
+            qhi0 = fmaxf(qhi0, b[3]), qhi1 = fmaxf(qhi1, b[4]), qhi2 = fmaxf(qhi2, b[5]);
+        }
+        const int64_t v0 = un.vbeg + (int64_t)tid * TP;
+        const int64_t v1 = min(v0 + TP, un.vend) - 1;  // last candidate position of the tile
+        int seg = 0, hi = un.ncell - 1;                 // last slot with s_vpre[slot] <= v0
+        while (seg < hi) {
+            const int mid = (seg + hi + 1) >> 1;
+            if (s_vpre[mid] <= v0) seg = mid; else hi = mid - 1;
+        }
+        float plo0 = INFINITY, plo1 = INFINITY, plo2 = INFINITY, phi0 = -INFINITY, phi1 = -INFINITY,
+              phi2 = -INFINITY;
+        for (; seg < un.ncell && s_vpre[seg] <= v1; ++seg) {
+            const int64_t pa = max(v0, (int64_t)s_vpre[seg]), pb = min(v1, (int64_t)s_vpre[seg + 1] - 1);
+            const int64_t ga = (s_nstart[seg] + (pa - s_vpre[seg])) >> 5;
+            const int64_t gb = (s_nstart[seg] + (pb - s_vpre[seg])) >> 5;
+            for (int64_t g = ga; g <= gb; ++g) {
+                const float4 l = __ldg(a.gbox + 2 * g), h = __ldg(a.gbox + 2 * g + 1);
+                plo0 = fminf(plo0, l.x), plo1 = fminf(plo1, l.y), plo2 = fminf(plo2, l.z);
+                phi0 = fmaxf(phi0, h.x), phi1 = fmaxf(phi1, h.y), phi2 = fmaxf(phi2, h.z);
+            }
+        }
+        const float g0 = fmaxf(0.f, fmaxf(__fsub_rn(plo0, qhi0), __fsub_rn(qlo0, phi0)));
+        const float g1 = fmaxf(0.f, fmaxf(__fsub_rn(plo1, qhi1), __fsub_rn(qlo1, phi1)));
+        const float g2 = fmaxf(0.f, fmaxf(__fsub_rn(plo2, qhi2), __fsub_rn(qlo2, phi2)));
+        keep = !(__fmaf_rn(g2, g2, __fmaf_rn(g1, g1, __fmul_rn(g0, g0))) > a.eps2);
+    }
+    // the kept tiles in increasing order: s_list[0 .. nkeep)
+    const uint32_t b = __ballot_sync(0xffffffffu, keep);
+    if (warp < 4 && lane == 0) s_keep[warp] = b;
+    __syncthreads();
+    int base = 0, nkeep = 0;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const int c = __popc(s_keep[w]);
+        base += w < warp ? c : 0;
+        nkeep += c;
+    }
+    if (keep) s_list[base + __popc(b & ((1u << lane) - 1u))] = (uint8_t)tid;
+    __syncthreads();
+    return nkeep;
+}
+
 // The producer warp: streams the unit's chunk through the stage ring.  Each
 // lane copies the 16-byte chunks of the staged dimensions (C4 chunks) of rows
 // lane and lane + 32 of a tile (cp.async), then arrives on the stage's full
@@ -553,12 +669,14 @@ __device__ __forceinline__ Unit unit_begin(const RefineArgs &a, int nst, uint64_
 template <int TP>
 __device__ __forceinline__ void produce(const RefineArgs &a, const Unit &un, float *P0, int32_t *s_row, int S, int C4,
                                         int d4, bool partial_rows, int nst, uint64_t *s_full, uint64_t *s_empty,
-                                        const int32_t *s_nstart, const int32_t *s_vpre, int lane)
+                                        const int32_t *s_nstart, const int32_t *s_vpre, const uint8_t *s_list,
+                                        int nkeep, int lane)
 {
-    for (int it = 0; it < un.ntiles; ++it) {
-        const int st = it % nst;
-        const uint32_t round = (uint32_t)(it / nst);
-        if (it >= nst && !refine_wait(&s_empty[st], (round - 1u) & 1u)) {
+    for (int slot = 0; slot < nkeep; ++slot) {
+        const int it = s_list[slot];
+        const int st = slot % nst;
+        const uint32_t round = (uint32_t)(slot / nst);
+        if (slot >= nst && !refine_wait(&s_empty[st], (round - 1u) & 1u)) {
             atomicExch(&a.flags[kFlagRefineTimeout], 1);
             return;
         }
@@ -618,6 +736,9 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
     __shared__ int32_t s_nstart[kStencil];
     __shared__ int32_t s_vpre[kStencil + 1];
     __shared__ int64_t s_info[2];
+    __shared__ __align__(16) float s_qbox[8 * kQueryWarps];
+    __shared__ uint32_t s_keep[4];
+    __shared__ uint8_t s_list[kCH / kTP];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d4 = D4 > 0 ? D4 : a.d4, S2 = pair_stride(d4);
@@ -635,15 +756,17 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
     uint32_t *s_sword = reinterpret_cast<uint32_t *>(s_sidx + kComputeWarps * kSurvMax);
 
     const Unit un = unit_begin<kTP>(a, nst, s_full, s_empty, s_nstart, s_vpre, s_info);
+    // staged tiles to stream and refine (slot i of the ring takes tile s_list[i])
+    const int nkeep = stage_keep<kTP, kTQ, 4 * MQ, PROF>(a, un, s_nstart, s_vpre, s_qbox, s_keep, s_list);
     const int64_t t = un.t;
     const int32_t q0 = un.q0;
     const int nq = un.nq;
     const int64_t W = un.W, W4 = un.W4;
     const int64_t vbeg = un.vbeg, vend = un.vend;
-    const int ntiles = un.ntiles;
 
     if (warp == kComputeWarps) {
-        produce<kTP>(a, un, P0, s_row, S, C4, d4, partial_rows, nst, s_full, s_empty, s_nstart, s_vpre, lane);
+        produce<kTP>(a, un, P0, s_row, S, C4, d4, partial_rows, nst, s_full, s_empty, s_nstart, s_vpre, s_list,
+                     nkeep, lane);
         return;
     }
 
@@ -672,10 +795,16 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
     uint32_t my_count = 0;                   // neighbours of query row qbase + 4 lp (lp < MQ)
     const int64_t row_word0 = a.tile_word[t] - a.word0;
     uint64_t prof_alg = 0, prof_exec = 0;
-    // box of the warp's query rows (wq * 4 MQ ... + 4 MQ - 1) over the three
-    // index dimensions; no query row: lo = +inf, hi = -inf
-    float qlo0, qlo1, qlo2, qhi0, qhi1, qhi2;
-    {
+    // Box of the warp's query rows (wq * 4 MQ ... + 4 MQ - 1) over the three
+    // index dimensions (no query row: lo = +inf, hi = -inf).  With 8 x 4
+    // blocks the warp reduces it into registers here; with 4 x 4 blocks it is
+    // read per tile from stage_keep's copy in shared memory, which leaves the
+    // registers to the larger survivor state.  Measured on GB300 (refinement):
+    // spectrum (d = 128) 342 ms with the shared-memory copy against 364;
+    // exp (d = 16) 12.1 s with registers against 12.3 s.
+    constexpr bool kQBoxRegs = MQ == 8;
+    float qlo0 = 0.f, qlo1 = 0.f, qlo2 = 0.f, qhi0 = 0.f, qhi1 = 0.f, qhi2 = 0.f;
+    if constexpr (kQBoxRegs) {
         const int r = wq * (4 * MQ) + (lane & (4 * MQ - 1));
         qlo0 = qlo1 = qlo2 = INFINITY;
         qhi0 = qhi1 = qhi2 = -INFINITY;
@@ -696,9 +825,10 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
         }
     }
 
-    for (int it = 0; it < ntiles; ++it) {
-        const int st = it % nst;
-        const uint32_t round = (uint32_t)(it / nst);
+    for (int slot = 0; slot < nkeep; ++slot) {
+        const int it = s_list[slot];
+        const int st = slot % nst;
+        const uint32_t round = (uint32_t)(slot / nst);
         if (!refine_wait(&s_full[st], round & 1u)) {
             atomicExch(&a.flags[kFlagRefineTimeout], 1);
             return;
@@ -716,12 +846,18 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
         // maxima; rows past the chunk end hold -inf, which only widens it.
         bool far = false;
         {
+            float blo0 = qlo0, blo1 = qlo1, blo2 = qlo2, bhi0 = qhi0, bhi1 = qhi1, bhi2 = qhi2;
+            if constexpr (!kQBoxRegs) {
+                const float4 qa = *reinterpret_cast<const float4 *>(s_qbox + 8 * wq);
+                const float4 qb = *reinterpret_cast<const float4 *>(s_qbox + 8 * wq + 4);
+                blo0 = qa.x, blo1 = qa.y, blo2 = qa.z, bhi0 = qa.w, bhi1 = qb.x, bhi2 = qb.y;
+            }
             const float4 c = *reinterpret_cast<const float4 *>(P + (wp * 32 + lane) * S);
             const float plo0 = warp_min(c.x), plo1 = warp_min(c.y), plo2 = warp_min(c.z);
             const float phi0 = warp_max(c.x), phi1 = warp_max(c.y), phi2 = warp_max(c.z);
-            const float g0 = fmaxf(0.f, fmaxf(__fsub_rn(plo0, qhi0), __fsub_rn(qlo0, phi0)));
-            const float g1 = fmaxf(0.f, fmaxf(__fsub_rn(plo1, qhi1), __fsub_rn(qlo1, phi1)));
-            const float g2 = fmaxf(0.f, fmaxf(__fsub_rn(plo2, qhi2), __fsub_rn(qlo2, phi2)));
+            const float g0 = fmaxf(0.f, fmaxf(__fsub_rn(plo0, bhi0), __fsub_rn(blo0, phi0)));
+            const float g1 = fmaxf(0.f, fmaxf(__fsub_rn(plo1, bhi1), __fsub_rn(blo1, phi1)));
+            const float g2 = fmaxf(0.f, fmaxf(__fsub_rn(plo2, bhi2), __fsub_rn(blo2, phi2)));
             far = __fmaf_rn(g2, g2, __fmaf_rn(g1, g1, __fmul_rn(g0, g0))) > eps2;
         }
         f32x2 acc[MQ / 2][MP];
@@ -816,7 +952,7 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
                         }
                         break;
                     }
-                    if (__all_sync(0xffffffffu, block_min<MQ, MP>(acc) > eps2)) {
+                    if (exit_check_at<MQ>(k, d4) && __all_sync(0xffffffffu, block_min<MQ, MP>(acc) > eps2)) {
                         any_close = false;
                         break;
                     }
