@@ -672,6 +672,12 @@ __device__ __forceinline__ void produce(const RefineArgs &a, const Unit &un, flo
                                         const int32_t *s_nstart, const int32_t *s_vpre, const uint8_t *s_list,
                                         int nkeep, int lane)
 {
+    // stencil slot of each of the lane's rows: positions only grow from one
+    // staged tile to the next, so the slot is found by walking forward from
+    // the previous one (usually no step in a large cell)
+    int seg[TP / 32];
+#pragma unroll
+    for (int h = 0; h < TP / 32; ++h) seg[h] = 0;
     for (int slot = 0; slot < nkeep; ++slot) {
         const int it = s_list[slot];
         const int st = slot % nst;
@@ -688,11 +694,9 @@ __device__ __forceinline__ void produce(const RefineArgs &a, const Unit &un, flo
             const int64_t v = v0 + r;
             float4 *row = reinterpret_cast<float4 *>(P + r * S);
             if (v < un.vend) {
-                int lo = 0, hi = un.ncell - 1;  // last slot with s_vpre[slot] <= v
-                while (lo < hi) {
-                    const int mid = (lo + hi + 1) >> 1;
-                    if (s_vpre[mid] <= v) lo = mid; else hi = mid - 1;
-                }
+                int lo = seg[h];  // last slot with s_vpre[slot] <= v
+                while (lo + 1 < un.ncell && s_vpre[lo + 1] <= v) ++lo;
+                seg[h] = lo;
                 const int32_t grow = s_nstart[lo] + (int32_t)(v - s_vpre[lo]);
                 const float *src = a.xs + (int64_t)grow * d4;
                 for (int cc = 0; cc < C4; ++cc) cp_async16(row + cc, src + 4 * cc);
