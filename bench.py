@@ -443,6 +443,11 @@ def run_config(args, cfg, world, rank, local, dist):
             "replicas": world,
             "pairs_per_step": pairs, "candidates_per_step": cand,
             "pruning": 1.0 - cand / float(n) ** 2,
+            # candidate pairs left after the refinement's group-box stage
+            # skip (the rest are proved farther than eps before streaming)
+            "candidates_refined_per_step": st.get("candidates_refined"),
+            "pruning_refined": (1.0 - st["candidates_refined"] / float(n) ** 2
+                                if st.get("candidates_refined", -1) >= 0 else None),
             "phase_ms": {k: st[k] for k in ("ms_build", "ms_index", "ms_count", "ms_refine", "ms_compact",
                                             "ms_deliver")},
             "batches": st["batches"], "deliveries": st["deliveries"], "cells": st["cells"], "clocks": clocks,

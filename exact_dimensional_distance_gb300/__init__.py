@@ -73,7 +73,8 @@ class hiss_stats(ctypes.Structure):
                 ("key_bits", _i32), ("eps", _f32), ("cell_width", ctypes.c_double),
                 ("ms_build", ctypes.c_double), ("ms_index", ctypes.c_double), ("ms_count", ctypes.c_double),
                 ("ms_refine", ctypes.c_double), ("ms_compact", ctypes.c_double),
-                ("ms_deliver", ctypes.c_double), ("ms_total", ctypes.c_double), ("deliveries", _i64)]
+                ("ms_deliver", ctypes.c_double), ("ms_total", ctypes.c_double), ("deliveries", _i64),
+                ("candidates_refined", _i64)]
 
 
 def _sig(name, res, args):

@@ -617,6 +617,10 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
 
     double ms_refine = 0.0, ms_compact = 0.0, ms_deliver = 0.0;
     int64_t pairs = 0, delivered = 0;
+    // candidate pairs of the staged tiles the CUDA-core refinement keeps,
+    // summed over the batches on the device (nb_d[4])
+    unsigned long long *kept_d = reinterpret_cast<unsigned long long *>(as<int64_t>(ctx->nb_d) + 4);
+    CK(cudaMemsetAsync(kept_d, 0, 8, s));
     // Hands over the overlapped delivery still in flight, if any.
     auto flush_pending = [&]() -> int {
         if (pending < 0) return HISS_OK;
@@ -669,6 +673,7 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
         ra.eps2 = eps * eps;
         ra.prof = nullptr;
         ra.gbox = as<float4>(ctx->gbox);
+        ra.kept = kept_d;
         ra.flags = as<int>(ctx->flags);
         if (!tc && chunk_major(ctx->d4)) {
             CK(unit_order(ra, qs.qcell_start, refine_tq(ctx->d4), as<int32_t>(ctx->unit_tile),
@@ -870,6 +875,10 @@ int run_batches(hiss_ctx *ctx, const QuerySide &qs, float eps, size_t batch_byte
     }
     ST(flush_pending());
     ST(check_flags(ctx));
+    int64_t kept = 0;
+    CK(cudaMemcpyAsync(&kept, kept_d, 8, cudaMemcpyDeviceToHost, s));
+    ST(sync(ctx));
+    ctx->st.candidates_refined = tc ? -1 : kept;
     ctx->st.pairs = mode == HISS_OUT_CSR ? pairs : -1;
     ctx->st.batches = nb;
     ctx->st.deliveries = delivered;
@@ -1017,6 +1026,7 @@ int do_semi(hiss_ctx *ctx, const float *d_queries, int64_t nq, float eps, size_t
     fill_grid_stats(ctx);
     ctx->st.pairs = 0;
     ctx->st.batches = 0;
+    ctx->st.candidates_refined = 0;
     if (nq == 0) return HISS_OK;
     CK(cudaEventRecord(ctx->ev[2], s));
     QuerySide qs;

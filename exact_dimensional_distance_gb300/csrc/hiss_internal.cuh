@@ -123,6 +123,7 @@ struct RefineArgs {
     float eps2;
     int64_t *prof;              // profile mode: [2] counters (sum of per-pair exit dims, executed dims)
     const float4 *gbox;         // boxes of xs's 32-row groups (see group_boxes); NULL: every staged tile is streamed
+    unsigned long long *kept;   // if set: candidate pairs of the staged tiles kept for refinement are added here
     int *flags;                 // device int[kNumFlags]; kFlagRefineTimeout set if a stage wait gave up
 };
 int refine_tq(int d4);

@@ -577,7 +577,8 @@ __device__ __forceinline__ Unit unit_begin(const RefineArgs &a, int nst, uint64_
 #endif
 template <int TP, int TQ, int QG, bool PROF>
 __device__ __forceinline__ int stage_keep(const RefineArgs &a, const Unit &un, const int32_t *s_nstart,
-                                          const int32_t *s_vpre, float *s_qbox, uint32_t *s_keep, uint8_t *s_list)
+                                          const int32_t *s_vpre, float *s_qbox, uint32_t *s_keep, uint8_t *s_list,
+                                          int *s_kept)
 {
     static_assert(kCH / TP <= 128 && TQ / 32 <= kComputeWarps && (QG == 16 || QG == 32), "keep mask geometry");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -606,9 +607,11 @@ __device__ __forceinline__ int stage_keep(const RefineArgs &a, const Unit &un, c
     }
     if (PROF || !HISS_STAGE_SKIP || a.gbox == nullptr) {
         if (tid < un.ntiles) s_list[tid] = (uint8_t)tid;
+        if (tid == 0 && a.kept) atomicAdd(a.kept, (unsigned long long)(un.vend - un.vbeg) * (unsigned long long)un.nq);
         __syncthreads();
         return un.ntiles;
     }
+    if (tid == 0) *s_kept = 0;
     __syncthreads();
     bool keep = false;
     if (tid < un.ntiles) {
@@ -643,6 +646,7 @@ __device__ __forceinline__ int stage_keep(const RefineArgs &a, const Unit &un, c
         const float g1 = fmaxf(0.f, fmaxf(__fsub_rn(plo1, qhi1), __fsub_rn(qlo1, phi1)));
         const float g2 = fmaxf(0.f, fmaxf(__fsub_rn(plo2, qhi2), __fsub_rn(qlo2, phi2)));
         keep = !(__fmaf_rn(g2, g2, __fmaf_rn(g1, g1, __fmul_rn(g0, g0))) > a.eps2);
+        if (keep && a.kept) atomicAdd(s_kept, (int)(v1 - v0 + 1));
     }
     // the kept tiles in increasing order: s_list[0 .. nkeep)
     const uint32_t b = __ballot_sync(0xffffffffu, keep);
@@ -657,6 +661,7 @@ __device__ __forceinline__ int stage_keep(const RefineArgs &a, const Unit &un, c
     }
     if (keep) s_list[base + __popc(b & ((1u << lane) - 1u))] = (uint8_t)tid;
     __syncthreads();
+    if (tid == 0 && a.kept) atomicAdd(a.kept, (unsigned long long)*s_kept * (unsigned long long)un.nq);
     return nkeep;
 }
 
@@ -743,6 +748,7 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
     __shared__ __align__(16) float s_qbox[8 * kQueryWarps];
     __shared__ uint32_t s_keep[4];
     __shared__ uint8_t s_list[kCH / kTP];
+    __shared__ int s_kept;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d4 = D4 > 0 ? D4 : a.d4, S2 = pair_stride(d4);
@@ -761,7 +767,7 @@ __global__ void __launch_bounds__(kRefineThreads, HISS_REFINE_MINB) k_refine(con
 
     const Unit un = unit_begin<kTP>(a, nst, s_full, s_empty, s_nstart, s_vpre, s_info);
     // staged tiles to stream and refine (slot i of the ring takes tile s_list[i])
-    const int nkeep = stage_keep<kTP, kTQ, 4 * MQ, PROF>(a, un, s_nstart, s_vpre, s_qbox, s_keep, s_list);
+    const int nkeep = stage_keep<kTP, kTQ, 4 * MQ, PROF>(a, un, s_nstart, s_vpre, s_qbox, s_keep, s_list, &s_kept);
     const int64_t t = un.t;
     const int32_t q0 = un.q0;
     const int nq = un.nq;

@@ -240,6 +240,10 @@ typedef struct {
     double ms_build, ms_index, ms_count, ms_refine, ms_compact, ms_deliver, ms_total;
     int64_t deliveries;             /* batches handed to the callback: more than batches when a batch's
                                        CSR result outgrew its share of batch_bytes and came in parts */
+    int64_t candidates_refined;     /* candidate pairs of the last join in the staged tiles the CUDA-core
+                                       refinement kept after its group-box test (at most candidates; the
+                                       rest were proved farther than eps without being streamed); -1 with
+                                       the tensor-core refinement */
 } hiss_stats;
 
 int hiss_last_stats(const hiss_ctx *ctx, hiss_stats *out);

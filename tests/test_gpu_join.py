@@ -66,6 +66,32 @@ def test_small_workloads(cfg, n, k):
     rows, counts, st = _join(x, eps)
     _check_rows(x, eps, rows)
     assert np.array_equal(counts, oracle.count_bound(x, eps))
+    # every result pair lies in a staged tile the refinement kept
+    assert st["pairs"] <= st["candidates_refined"] <= st["candidates"]
+
+
+def test_stage_skip_keeps_every_neighbour():
+    """Points spread along one axis (the other dimensions nearly constant):
+    a 128-query tile covers part of its cell, so the 32-row groups at the far
+    ends of the neighbouring cells are more than eps from it and their tiles
+    are skipped before streaming.  The result must not change, and the
+    tensor-core refinement (which streams every tile) reports -1."""
+    rng = np.random.default_rng(5)
+    n, d = 4096, 16
+    x = rng.normal(0.0, 0.01, (n, d)).astype(np.float32)
+    x[:, 0] = rng.uniform(0.0, 10.0, n).astype(np.float32)
+    eps = 1.0
+    rows, counts, st = _join(x, eps)
+    _check_rows(x, eps, rows)
+    assert st["pairs"] <= st["candidates_refined"] < st["candidates"]
+    edd = _edd()
+    j = edd.Join()
+    j.build(torch.from_numpy(x).cuda())
+    j.set_refine(True)
+    rows_tc = j.join_sets(eps, 0)
+    assert j.stats()["candidates_refined"] == -1
+    j.close()
+    _check_rows(x, eps, rows_tc)
 
 
 @pytest.mark.parametrize("d", [1, 2, 3, 5, 17, 64, 127, 128, 130, 200, 256])
