@@ -145,8 +145,11 @@ typedef struct {
  * one query tile, or one query's row of results, does not fit.  Each batch is
  * refined exactly on CUDA cores (float32 squared distances summed in
  * variance order, pair rejected once the partial sum exceeds eps^2; bit =
- * sum <= eps^2), compacted from the mask to CSR (Section IV-F1) unless
- * out->mode is HISS_OUT_MASK, and handed to out->on_batch.  Every query
+ * sum <= eps^2; candidate tiles whose boxes over the index dimensions are
+ * provably farther than eps from the query tile's box are skipped with
+ * their bits 0, see hiss_stats.candidates_refined), compacted from the mask
+ * to CSR (Section IV-F1) unless out->mode is HISS_OUT_MASK, and handed to
+ * out->on_batch.  Every query
  * appears in exactly one batch; every row contains the query itself.
  * batch_bytes = 0 selects 1/4 of the free device memory.  out may be NULL
  * (CSR, device, no callback).
