@@ -45,7 +45,10 @@ def test_semi_join_matches_oracle(cfg, nd, nq, eps):
     qd = torch.from_numpy(xq).cuda()
     counts = j.count_queries(qd, eps).cpu().numpy()
     rows = j.join_queries_sets(qd, eps)
+    st = j.stats()
     j.close()
+    # the stage skip keeps every result pair's tile
+    assert st["pairs"] <= st["candidates_refined"] <= st["candidates"]
     assert np.array_equal(counts, oracle.semi_count_bound(xq, xd, eps))
     _check(xq, xd, eps, rows)
     true = np.array([len(rows[r]) for r in range(nq)])
@@ -101,6 +104,7 @@ def test_semi_join_edge_cases_and_batching():
     st2 = j.stats()
     j.close()
     assert st1["batches"] == 1 and st2["batches"] > 2
+    assert st1["candidates_refined"] == st2["candidates_refined"]  # batching does not change the skip
     for r in range(len(xq)):
         assert np.array_equal(np.sort(one[r]), np.sort(many[r]))
     _check(xq[::29], xd, 0.7, {i: one[r] for i, r in enumerate(range(0, len(xq), 29))})
