@@ -1110,11 +1110,16 @@ __global__ void __launch_bounds__(kCompactWarps * 32) k_compact(const CompactArg
     int32_t *out = a.cols + (a.row_ptr[gq] - a.col0);
     int64_t run = 0;
     const int64_t o0 = woff >> 5, o1 = (woff + W - 1) >> 5;
+    // occupancy words are loaded two sweeps ahead, so that their latency
+    // overlaps the mask-word work of the current sweep
+    uint32_t ahead0 = o0 + lane <= o1 ? a.occ[o0 + lane] : 0u;
+    uint32_t ahead1 = o0 + 32 + lane <= o1 ? a.occ[o0 + 32 + lane] : 0u;
     for (int64_t ob = o0; ob <= o1; ob += 32) {
         const int64_t o = ob + lane;
-        uint32_t bits = 0;
+        uint32_t bits = ahead0;
+        ahead0 = ahead1;
+        ahead1 = o + 64 <= o1 ? a.occ[o + 64] : 0u;
         if (o <= o1) {
-            bits = a.occ[o];
             const int64_t wlo = 32 * o;
             if (wlo < woff) bits &= ~0u << (int)(woff - wlo);
             const int64_t n_in = woff + W - wlo;
